@@ -1,0 +1,340 @@
+// HBM-bound kernels of the update phase (sm_103a):
+//   f0 momentum           (SS-HSDP section 3.1 EG1; Figure 4 "Local momentum g, m -> u (BF16)")
+//   fragment gather       (section 3.2 "Distributed updates"; section 3.4: the execution
+//                          rank gathers the missing u fragments)
+//   f2 update + scatter   (EG1; section 3.4: v fragments return to their owners, which
+//                          update their main-weight fragments)
+//   G MXFP8 requant       (EG1; Figure 4 "UE8M0", "K-major scale layout"; OCP MX format)
+//   AdamW                 (section 5.2: AdamW updates the parameters Muon does not)
+//
+// Every kernel streams a virtual index space described by a range table
+// (hm::Range): consecutive ranges map one index space onto the segments of
+// the emulated rank allocation.  A CTA takes kTile consecutive indices,
+// finds its first range by binary search and walks forward; every thread
+// moves 16-byte vectors.  Range lengths are multiples of 32 elements, so a
+// vector never crosses a range and a 1x32 MX block never crosses a segment.
+#include "hm_internal.h"
+
+#include <cuda_bf16.h>
+
+namespace hm {
+
+__device__ int32_t g_error_word;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int64_t kTile = 16384;  // elements per CTA tile
+
+__device__ __forceinline__ const Range& range_at(const RangeArgs& ra, int i) {
+    return ra.tab ? ra.tab[i] : ra.inl[i];
+}
+
+__device__ __forceinline__ int find_range(const RangeArgs& ra, int64_t v) {
+    int lo = 0, hi = ra.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (range_at(ra, mid).prefix <= v) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+int grid_for(int64_t total) {
+    const int64_t tiles = (total + kTile - 1) / kTile;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+    return static_cast<int>(tiles < cap ? tiles : cap);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    return a | (b << 16);
+}
+
+// ---------------------------------------------------------------------------
+// f0: m <- mu*m + g (fp32, multiply then add, each rounded); u = bf16_RNE(m)
+// (Nesterov: u = bf16_RNE(g + mu*m_new)).  8 elements per thread step.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) f0_kernel(const __grid_constant__ RangeArgs ra, float* __restrict__ m,
+                                                       const float* __restrict__ g, uint16_t* __restrict__ u,
+                                                       float mu, int nesterov) {
+    for (int64_t t0 = blockIdx.x * kTile; t0 < ra.total; t0 += static_cast<int64_t>(gridDim.x) * kTile) {
+        int ri = find_range(ra, t0);
+        const int64_t t1 = min(t0 + kTile, ra.total);
+        for (int64_t v = t0 + threadIdx.x * 8; v < t1; v += kThreads * 8) {
+            while (v >= range_at(ra, ri).prefix + range_at(ra, ri).len) ++ri;
+            const Range& r = range_at(ra, ri);
+            const int64_t e = r.a + (v - r.prefix);
+            const float4* gp = reinterpret_cast<const float4*>(g + e);
+            float4* mp = reinterpret_cast<float4*>(m + e);
+            float4 g0 = __ldcs(gp), g1 = __ldcs(gp + 1);
+            float4 m0 = __ldcs(mp), m1 = __ldcs(mp + 1);
+            float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            float src[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                mv[k] = __fadd_rn(__fmul_rn(mu, mv[k]), gv[k]);
+                src[k] = nesterov ? __fadd_rn(gv[k], __fmul_rn(mu, mv[k])) : mv[k];
+            }
+            __stcs(mp, make_float4(mv[0], mv[1], mv[2], mv[3]));
+            __stcs(mp + 1, make_float4(mv[4], mv[5], mv[6], mv[7]));
+            uint4 pk = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]),
+                                  pack_bf16x2(src[4], src[5]), pack_bf16x2(src[6], src[7]));
+            *reinterpret_cast<uint4*>(u + e) = pk;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Fragment gather: bit copy of bf16 fragments, range.a -> range.b.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) copy_bf16_kernel(const __grid_constant__ RangeArgs ra,
+                                                             const uint16_t* __restrict__ src,
+                                                             uint16_t* __restrict__ dst) {
+    for (int64_t t0 = blockIdx.x * kTile; t0 < ra.total; t0 += static_cast<int64_t>(gridDim.x) * kTile) {
+        int ri = find_range(ra, t0);
+        const int64_t t1 = min(t0 + kTile, ra.total);
+        for (int64_t v = t0 + threadIdx.x * 8; v < t1; v += kThreads * 8) {
+            while (v >= range_at(ra, ri).prefix + range_at(ra, ri).len) ++ri;
+            const Range& r = range_at(ra, ri);
+            const int64_t d = v - r.prefix;
+            const uint4 x = __ldcs(reinterpret_cast<const uint4*>(src + r.a + d));
+            __stcg(reinterpret_cast<uint4*>(dst + r.b + d), x);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// f2 fused with the return of v fragments: w[a+d] <- w*decay - step * v[b+d],
+// v read from the v root (local units) or the staging (flag bit 0).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) f2_kernel(const __grid_constant__ RangeArgs ra, float* __restrict__ w,
+                                                       const float* __restrict__ v_root,
+                                                       const float* __restrict__ v_stage, float decay,
+                                                       int has_decay) {
+    for (int64_t t0 = blockIdx.x * kTile; t0 < ra.total; t0 += static_cast<int64_t>(gridDim.x) * kTile) {
+        int ri = find_range(ra, t0);
+        const int64_t t1 = min(t0 + kTile, ra.total);
+        for (int64_t v = t0 + threadIdx.x * 8; v < t1; v += kThreads * 8) {
+            while (v >= range_at(ra, ri).prefix + range_at(ra, ri).len) ++ri;
+            const Range& r = range_at(ra, ri);
+            const int64_t d = v - r.prefix;
+            const float* vp = ((r.flags & 1) ? v_stage : v_root) + r.b + d;
+            float4* wp = reinterpret_cast<float4*>(w + r.a + d);
+            const float step = r.step;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float4 x = __ldcs(wp + h);
+                const float4 y = __ldcs(reinterpret_cast<const float4*>(vp) + h);
+                if (has_decay) {
+                    x.x = __fmul_rn(x.x, decay); x.y = __fmul_rn(x.y, decay);
+                    x.z = __fmul_rn(x.z, decay); x.w = __fmul_rn(x.w, decay);
+                }
+                x.x = __fsub_rn(x.x, __fmul_rn(step, y.x));
+                x.y = __fsub_rn(x.y, __fmul_rn(step, y.y));
+                x.z = __fsub_rn(x.z, __fmul_rn(step, y.z));
+                x.w = __fsub_rn(x.w, __fmul_rn(step, y.w));
+                wp[h] = x;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// G: MXFP8 requant.  Four lanes own one 1x32 block (8 elements each); the
+// block amax is reduced with two xor-shuffles.  Scale exponent
+// e = clamp(floor(log2 amax) - 8, -127, 127) read from the fp32 bit pattern
+// (exact, subnormals included); elements y = x * 2^-e (a power of two: exact
+// whenever y is in E4M3 range) are rounded to E4M3 by the hardware's
+// round-to-nearest-even, saturate-to-finite conversion.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int mx_scale_exponent(float amax) {
+    const uint32_t bits = __float_as_uint(amax);
+    const int ex = static_cast<int>(bits >> 23);
+    int fl;
+    if (ex == 0) {
+        const uint32_t mant = bits & 0x7FFFFFu;
+        if (mant == 0) return -127;
+        fl = (31 - __clz(static_cast<int>(mant))) - 149;
+    } else {
+        fl = ex - 127;
+    }
+    const int e = fl - 8;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads) requant_kernel(const __grid_constant__ RangeArgs ra,
+                                                           const float* __restrict__ w, uint8_t* __restrict__ q,
+                                                           uint8_t* __restrict__ s) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    for (int64_t t0 = blockIdx.x * kTile; t0 < ra.total; t0 += static_cast<int64_t>(gridDim.x) * kTile) {
+        int ri = find_range(ra, t0);
+        const int64_t t1 = min(t0 + kTile, ra.total);
+        // warp-uniform loop: a warp covers 256 consecutive indices (8 blocks)
+        for (int64_t wb = t0 + warp * 256; wb < t1; wb += kThreads * 8) {
+            const int64_t v = wb + lane * 8;
+            const bool live = v < t1;  // uniform across the 4 lanes of a block
+            float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const Range* r = nullptr;
+            if (live) {
+                while (v >= range_at(ra, ri).prefix + range_at(ra, ri).len) ++ri;
+                r = &range_at(ra, ri);
+                const float4* p = reinterpret_cast<const float4*>(w + r->a + (v - r->prefix));
+                const float4 a = __ldcs(p), b = __ldcs(p + 1);
+                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            if (live) {
+                const int e = mx_scale_exponent(amax);
+                const float sc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, normal
+                const uint32_t c01 = cvt_e4m3x2(x[0] * sc, x[1] * sc);
+                const uint32_t c23 = cvt_e4m3x2(x[2] * sc, x[3] * sc);
+                const uint32_t c45 = cvt_e4m3x2(x[4] * sc, x[5] * sc);
+                const uint32_t c67 = cvt_e4m3x2(x[6] * sc, x[7] * sc);
+                const int64_t d = v - r->prefix;
+                uint2 pk = make_uint2(c01 | (c23 << 16), c45 | (c67 << 16));
+                __stcs(reinterpret_cast<uint2*>(q + r->b + d), pk);
+                if ((lane & 3) == 0) s[(r->c + d) >> 5] = static_cast<uint8_t>(e + 127);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// AdamW (decoupled weight decay, bias-corrected), 4 elements per thread step;
+// the scalar tail (n % 4) is handled by the first threads of block 0.
+// ---------------------------------------------------------------------------
+struct AdamArgs {
+    float b1, b2, eps, decay, step_size, inv_sqrt_bc2;
+};
+
+__device__ __forceinline__ void adam_elem(float& w, float g, float& m, float& v, const AdamArgs& a) {
+    w = w * a.decay;
+    m = a.b1 * m + (1.f - a.b1) * g;
+    v = a.b2 * v + (1.f - a.b2) * (g * g);
+    const float denom = sqrtf(v) * a.inv_sqrt_bc2 + a.eps;
+    w = w - a.step_size * (m / denom);
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kThreads) adamw_kernel(float* __restrict__ w, const void* __restrict__ gv,
+                                                         float* __restrict__ m, float* __restrict__ v, int64_t n,
+                                                         AdamArgs a) {
+    const int64_t nv = n / 4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < nv; i += stride) {
+        float4 wv = __ldcs(reinterpret_cast<const float4*>(w) + i);
+        float4 mv = __ldcs(reinterpret_cast<const float4*>(m) + i);
+        float4 vv = __ldcs(reinterpret_cast<const float4*>(v) + i);
+        float g[4];
+        if (kBf16) {
+            const uint2 gb = __ldcs(reinterpret_cast<const uint2*>(gv) + i);
+            g[0] = __uint_as_float(gb.x << 16);
+            g[1] = __uint_as_float(gb.x & 0xFFFF0000u);
+            g[2] = __uint_as_float(gb.y << 16);
+            g[3] = __uint_as_float(gb.y & 0xFFFF0000u);
+        } else {
+            const float4 gf = __ldcs(reinterpret_cast<const float4*>(gv) + i);
+            g[0] = gf.x; g[1] = gf.y; g[2] = gf.z; g[3] = gf.w;
+        }
+        adam_elem(wv.x, g[0], mv.x, vv.x, a);
+        adam_elem(wv.y, g[1], mv.y, vv.y, a);
+        adam_elem(wv.z, g[2], mv.z, vv.z, a);
+        adam_elem(wv.w, g[3], mv.w, vv.w, a);
+        __stcs(reinterpret_cast<float4*>(w) + i, wv);
+        __stcs(reinterpret_cast<float4*>(m) + i, mv);
+        __stcs(reinterpret_cast<float4*>(v) + i, vv);
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n & 3)) {
+        const int64_t j = nv * 4 + threadIdx.x;
+        float g = kBf16 ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(gv)[j]) << 16)
+                        : reinterpret_cast<const float*>(gv)[j];
+        adam_elem(w[j], g, m[j], v[j], a);
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+int device_sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 148;
+    }
+    return cached[dev];
+}
+
+int32_t* device_error_word() {
+    static void* cached[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cached[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+        cached[dev] = p;
+    }
+    return static_cast<int32_t*>(cached[dev]);
+}
+
+cudaError_t launch_f0(const RangeArgs& ra, float* m, const float* g, uint16_t* u, float mu, int nesterov,
+                      cudaStream_t st) {
+    if (ra.total == 0) return cudaSuccess;
+    f0_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, m, g, u, mu, nesterov);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_bf16(const RangeArgs& ra, const uint16_t* src, uint16_t* dst, cudaStream_t st) {
+    if (ra.total == 0) return cudaSuccess;
+    copy_bf16_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, src, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_f2(const RangeArgs& ra, float* w, const float* v_root, const float* v_stage, float decay,
+                      int has_decay, cudaStream_t st) {
+    if (ra.total == 0) return cudaSuccess;
+    f2_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, w, v_root, v_stage, decay, has_decay);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_requant(const RangeArgs& ra, const float* w, uint8_t* q, uint8_t* s, cudaStream_t st) {
+    if (ra.total == 0) return cudaSuccess;
+    requant_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, w, q, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adamw(float* w, const void* g, int g_bf16, float* m, float* v, int64_t n, float lr, float beta1,
+                         float beta2, float eps, float decay, float step_size, float inv_sqrt_bc2, cudaStream_t st) {
+    (void)lr;
+    if (n == 0) return cudaSuccess;
+    AdamArgs a{beta1, beta2, eps, decay, step_size, inv_sqrt_bc2};
+    const int64_t nv = n / 4;
+    int64_t blocks = (nv + kThreads - 1) / kThreads;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (g_bf16)
+        adamw_kernel<true><<<static_cast<int>(blocks), kThreads, 0, st>>>(w, g, m, v, n, a);
+    else
+        adamw_kernel<false><<<static_cast<int>(blocks), kThreads, 0, st>>>(w, g, m, v, n, a);
+    return cudaGetLastError();
+}
+
+}  // namespace hm

@@ -1,0 +1,114 @@
+// Internal declarations shared by the host planner (hm_host.cpp) and the
+// CUDA kernels (hm_elementwise.cu, hm_ns.cu).  Not part of the C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace hm {
+
+// Device-side error codes recorded in the library's device error word.
+constexpr int kDevErrTimeout = -9;   // == HM_ERR_TIMEOUT
+
+// One entry of a range table: the same element index d in [0, len) maps to
+// element a + d of one buffer, b + d of another and, for MXFP8 scales,
+// (c + d) / 32 of a third.  `prefix` is the exclusive prefix sum of len over
+// the table, so a table describes one virtual index space [0, total).
+struct Range {
+    int64_t a;
+    int64_t b;
+    int64_t c;
+    int64_t len;
+    int64_t prefix;
+    float   step;   // f2: fp32(lr * alpha) of the unit the range belongs to
+    int32_t flags;  // f2: bit 0 = v read from the workspace staging
+};
+static_assert(sizeof(Range) == 48, "Range layout");
+
+constexpr int kInlineRanges = 32;
+
+// Kernel argument: a table either in device memory (tab != nullptr) or
+// inline in the kernel's parameter space.
+struct RangeArgs {
+    const Range* tab;
+    int32_t n;
+    int32_t pad;
+    int64_t total;
+    Range inl[kInlineRanges];
+};
+
+// One Newton-Schulz unit.
+struct NsUnit {
+    int64_t u_off;   // element offset of u in the u root or the u staging
+    int64_t v_off;   // element offset of v in the v root or the v staging
+    int32_t rows;    // unit as stored: rows x cols, row-major
+    int32_t cols;
+    int32_t flags;   // kNsU* bits
+    int32_t pad;
+};
+static_assert(sizeof(NsUnit) == 32, "NsUnit layout");
+constexpr int kNsUStaged = 1;       // u read from staging
+constexpr int kNsVStaged = 2;       // v written to staging
+constexpr int kNsTransposed = 4;    // rows > cols: X = u^T
+
+// A Newton-Schulz shape class: units with the same (m, n) = (min, max) of
+// (rows, cols).  X is stored padded to mp x np (mp multiple of 128, np
+// multiple of 64) with zeros outside m x n; the zero padding stays zero
+// through every iteration.
+struct NsClassDev {
+    int32_t m, n, mp, np;
+    int32_t n_units;
+    int32_t first_unit;  // into the NsUnit table
+    int32_t parts;       // norm partial sums per unit
+    int32_t part_len;    // elements per partial (multiple of 8)
+    size_t x_off[2], xt_off[2], a_off, b_off, part_off, inv_off;  // workspace bytes
+};
+
+// Epilogue kinds of the Newton-Schulz GEMM.
+enum GemmEpi : int {
+    kEpiGram = 0,    // out = bf16(acc)                         (A = X X^T)
+    kEpiPoly = 1,    // out = bf16(alpha*acc + beta*add)        (B = b A + c A A)
+    kEpiUpdate = 2,  // out = out_t^T = bf16(acc + beta*add)    (X = a X + B X)
+    kEpiFinal = 3,   // v   = fp32(acc + beta*add), per-unit destination
+};
+
+struct GemmParams {
+    int32_t M, N, K;            // per unit; M multiple of 128, N multiple of 32
+    int32_t units, tiles_m, tiles_n, num_kb;
+    int32_t epi;
+    float alpha, beta;
+    uint16_t* out;       int64_t out_us;   int32_t ld_out;   // [units][M][N]
+    uint16_t* out_t;     int64_t out_t_us; int32_t ld_out_t; // [units][N][M]
+    const uint16_t* add; int64_t add_us;   int32_t ld_add;   // [units][M][N]
+    const NsUnit* ns_units;                                   // final: destinations
+    float* v_root;
+    float* v_stage;
+    int32_t m_real, n_real;
+    int32_t* err;
+};
+
+// ---- launchers (return cudaGetLastError() of the launch) -----------------
+int device_sm_count();
+int32_t* device_error_word();
+
+cudaError_t launch_f0(const RangeArgs& ra, float* m, const float* g, uint16_t* u, float mu,
+                      int nesterov, cudaStream_t st);
+cudaError_t launch_copy_bf16(const RangeArgs& ra, const uint16_t* src, uint16_t* dst, cudaStream_t st);
+cudaError_t launch_f2(const RangeArgs& ra, float* w, const float* v_root, const float* v_stage,
+                      float decay, int has_decay, cudaStream_t st);
+cudaError_t launch_requant(const RangeArgs& ra, const float* w, uint8_t* q, uint8_t* s, cudaStream_t st);
+cudaError_t launch_adamw(float* w, const void* g, int g_bf16, float* m, float* v, int64_t n,
+                         float lr, float beta1, float beta2, float eps, float decay,
+                         float step_size, float inv_sqrt_bc2, cudaStream_t st);
+
+cudaError_t launch_ns_norm(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
+                           const uint16_t* u_stage, char* ws, float eps, cudaStream_t st);
+cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
+                              const uint16_t* u_stage, char* ws, cudaStream_t st);
+cudaError_t launch_ns_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p,
+                           int bn, cudaStream_t st);
+
+}  // namespace hm

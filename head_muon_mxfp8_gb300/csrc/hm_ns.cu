@@ -1,0 +1,511 @@
+// f1: batched Newton-Schulz on sm_103a tensor cores.
+//
+// SS-HSDP section 3.1 (example EG1: f1 applies Newton-Schulz to the complete
+// BF16 intermediate u and writes the FP32 direction v to separate scratch) and
+// section 4.1 (f1 groups matrices with matching shapes for batched GEMMs).
+// Per unit (rows x cols, m = min, n = max):
+//   X0 = u / (||u||_F + eps), taken as u^T when rows > cols (m x n);
+//   repeat: A = X X^T;  B = b A + c A A;  X = a X + B X;
+//   v = X (transposed back).
+// A, B and X are rounded to bf16 after each product (fp32 accumulation in
+// TMEM); the last product is written to v in fp32.
+//
+// Layout in the workspace, per shape class of U units:
+//   X[2], XT[2]  bf16 [U][mp][np] / [U][np][mp]   (ping-pong; XT = X^T)
+//   A, B         bf16 [U][mp][mp]
+// with mp = m rounded up to 128 and np = n rounded up to 64; the padding is
+// zero and stays zero.  Keeping X and X^T both row-major lets every GEMM read
+// both operands K-major: A = X X^T contracts X rows with X rows, A A
+// contracts A rows with A rows (A is symmetric), B X contracts B rows with
+// X^T rows.
+//
+// GEMM kernel: persistent, one CTA per SM, 192 threads:
+//   warp 0      TMA producer: 128x64 and BNx64 bf16 boxes, 128-byte swizzle,
+//               STAGES-deep mbarrier ring;
+//   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=16)
+//               from one lane into a double-buffered fp32 accumulator;
+//   warps 2-5   epilogue: tcgen05.ld 32x32b rows out of TMEM, fused
+//               element-wise tail, global stores.
+// Every mbarrier wait is bounded (2 s of %globaltimer); on timeout the CTA
+// records HM_ERR_TIMEOUT in the device error word, lets every role finish,
+// waits for its own TMA copies and MMAs, frees TMEM and returns.
+#include "hm_internal.h"
+
+#include <cuda_bf16.h>
+
+namespace hm {
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Frobenius norm: per-unit partial sums of squares, then 1 / (sqrt + eps).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) ns_norm_partial_kernel(const NsUnit* __restrict__ units,
+                                                               const uint16_t* __restrict__ u_root,
+                                                               const uint16_t* __restrict__ u_stage,
+                                                               float* __restrict__ partials, int parts,
+                                                               int part_len) {
+    const NsUnit nu = units[blockIdx.y];
+    const uint16_t* src = ((nu.flags & kNsUStaged) ? u_stage : u_root) + nu.u_off;
+    const int64_t numel = static_cast<int64_t>(nu.rows) * nu.cols;
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * part_len;
+    const int64_t b1 = min(b0 + part_len, numel);
+    float acc = 0.f;
+    for (int64_t i = b0 + threadIdx.x * 8; i < b1; i += 256 * 8) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(src + i));
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+            acc = fmaf(lo, lo, acc);
+            acc = fmaf(hi, hi, acc);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    __shared__ float red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = 0.f;
+        for (int k = 0; k < 8; ++k) s += red[k];
+        partials[static_cast<int64_t>(blockIdx.y) * parts + blockIdx.x] = s;
+    }
+}
+
+__global__ void ns_norm_final_kernel(const float* __restrict__ partials, int parts, float* __restrict__ inv,
+                                     float eps, int n_units) {
+    const int unit = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (unit >= n_units) return;
+    float s = 0.f;
+    for (int k = lane; k < parts; k += 32) s += partials[static_cast<int64_t>(unit) * parts + k];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) inv[unit] = 1.0f / (sqrtf(s) + eps);
+}
+
+// ---------------------------------------------------------------------------
+// X0 and X0^T from u: 64x64 tiles of X coordinates through shared memory,
+// coalesced reads of u in either orientation, coalesced writes of X and X^T.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) ns_prepare_kernel(const NsUnit* __restrict__ units,
+                                                          const uint16_t* __restrict__ u_root,
+                                                          const uint16_t* __restrict__ u_stage,
+                                                          const float* __restrict__ inv, uint16_t* __restrict__ X,
+                                                          uint16_t* __restrict__ XT, int m, int n, int mp, int np) {
+    __shared__ uint16_t T[64][66];
+    const int unit = blockIdx.z;
+    const NsUnit nu = units[unit];
+    const uint16_t* src = ((nu.flags & kNsUStaged) ? u_stage : u_root) + nu.u_off;
+    const bool tr = nu.flags & kNsTransposed;
+    const float s = inv[unit];
+    const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+    for (int idx = threadIdx.x; idx < 64 * 64; idx += 256) {
+        int ii, jj;
+        if (!tr) { ii = idx >> 6; jj = idx & 63; }
+        else { jj = idx >> 6; ii = idx & 63; }
+        const int i = i0 + ii, j = j0 + jj;
+        uint16_t val = 0;
+        if (i < m && j < n) {
+            const uint16_t raw = tr ? src[static_cast<int64_t>(j) * m + i] : src[static_cast<int64_t>(i) * n + j];
+            val = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(static_cast<uint32_t>(raw) << 16) * s));
+        }
+        T[ii][jj] = val;
+    }
+    __syncthreads();
+    uint16_t* xo = X + static_cast<int64_t>(unit) * mp * np;
+    uint16_t* to = XT + static_cast<int64_t>(unit) * mp * np;
+    for (int idx = threadIdx.x; idx < 64 * 64; idx += 256) {
+        const int ii = idx >> 6, jj = idx & 63;
+        xo[static_cast<int64_t>(i0 + ii) * np + j0 + jj] = T[ii][jj];
+    }
+    for (int idx = threadIdx.x; idx < 64 * 64; idx += 256) {
+        const int jj = idx >> 6, ii = idx & 63;
+        to[static_cast<int64_t>(j0 + jj) * mp + i0 + ii] = T[ii][jj];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier, TMA, tcgen05
+// ---------------------------------------------------------------------------
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kGemmThreads = 192;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait.  Gives up when another role of the CTA has given up (bail)
+// or after kWaitNs; the first give-up records HM_ERR_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err, volatile int* bail,
+                                          bool honour_bail = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (honour_bail && *bail) return false;
+        if (globaltimer() - t0 > kWaitNs) {
+            *bail = 1;
+            if (err) atomicCAS(err, 0, kDevErrTimeout);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with the 128-byte swizzle: rows of 64 bf16 (128 B), 8-row atoms of 1024 B
+// (stride-dimension byte offset 1024), descriptor version 1, swizzle mode
+// "128B".  Advancing K by 16 elements adds 32 bytes to the start address.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
+    // kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major,
+    // N >> 3 at bit 17, M >> 4 at bit 24.
+    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+                                      (static_cast<uint32_t>(BN >> 3) << 17) |
+                                      (static_cast<uint32_t>(BM >> 4) << 24);
+};
+
+__device__ __forceinline__ void decode_tile(int t, const GemmParams& p, int& u, int& tm, int& tn) {
+    const int per = p.tiles_m * p.tiles_n;
+    u = t / per;
+    const int r = t - u * per;
+    const int group = 8 * p.tiles_n;
+    const int g = r / group;
+    const int first = g * 8;
+    const int gm = min(p.tiles_m - first, 8);
+    const int rr = r - g * group;
+    tm = first + rr % gm;
+    tn = rr / gm;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& x, float* f) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        f[2 * k] = __uint_as_float(w[k] << 16);
+        f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+}
+__device__ __forceinline__ uint32_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm, int tn, int row, uint32_t taddr) {
+    const int i = tm * BM + row;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        const int j0 = tn * BN + c * 32;
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        tmem_ld_wait();
+        if (j0 >= p.N) continue;  // warp-uniform; N is a multiple of 32
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * p.alpha;
+        if (p.epi != kEpiGram) {
+            const uint4* ap = reinterpret_cast<const uint4*>(p.add + u * p.add_us + static_cast<int64_t>(i) * p.ld_add + j0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float a8[8];
+                unpack_bf16x8(__ldg(ap + q), a8);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[q * 8 + k] = fmaf(p.beta, a8[k], v[q * 8 + k]);
+            }
+        }
+        if (p.epi == kEpiFinal) {
+            const NsUnit nu = p.ns_units[u];
+            if (i < p.m_real) {
+                float* dst = ((nu.flags & kNsVStaged) ? p.v_stage : p.v_root) + nu.v_off;
+                if (nu.flags & kNsTransposed) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        if (j0 + k < p.n_real) dst[static_cast<int64_t>(j0 + k) * p.m_real + i] = v[k];
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        if (j0 + k < p.n_real) dst[static_cast<int64_t>(i) * p.n_real + j0 + k] = v[k];
+                }
+            }
+            continue;
+        }
+        uint4 pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            pk[q] = make_uint4(bf16_bits(v[8 * q + 0]) | (bf16_bits(v[8 * q + 1]) << 16),
+                               bf16_bits(v[8 * q + 2]) | (bf16_bits(v[8 * q + 3]) << 16),
+                               bf16_bits(v[8 * q + 4]) | (bf16_bits(v[8 * q + 5]) << 16),
+                               bf16_bits(v[8 * q + 6]) | (bf16_bits(v[8 * q + 7]) << 16));
+        uint4* op = reinterpret_cast<uint4*>(p.out + u * p.out_us + static_cast<int64_t>(i) * p.ld_out + j0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) op[q] = pk[q];
+        if (p.epi == kEpiUpdate) {
+            uint16_t* tp = p.out_t + u * p.out_t_us + static_cast<int64_t>(j0) * p.ld_out_t + i;
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(pk);
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                tp[static_cast<int64_t>(k) * p.ld_out_t] = static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
+        }
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    ns_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
+                   const __grid_constant__ GemmParams p) {
+    using C = GemmCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sa = smem;
+    uint8_t* sb = sa + C::STAGES * C::A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sb + C::STAGES * C::B_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* tfull = bars + 2 * C::STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* bail = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tfull[b]), 1);
+            mbar_init(smem_u32(&tempty[b]), 128);
+        }
+        mbar_init(smem_u32(drain), 1);
+        *bail = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int total = p.units * p.tiles_m * p.tiles_n;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, armed = 0, armed_par = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                int u, tm, tn;
+                decode_tile(t, p, u, tm, tn);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, p.err, bail)) { ok = false; break; }
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+                    tma_load_3d(smem_u32(sa + s * C::A_BYTES), &tma, fb, kb * BK, tm * BM, u);
+                    tma_load_3d(smem_u32(sb + s * C::B_BYTES), &tmb, fb, kb * BK, tn * BN, u);
+                    armed |= 1u << s;
+                    armed_par = (armed_par & ~(1u << s)) | (ph << s);
+                    if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+                }
+            }
+            // wait for this CTA's own copies still in flight
+            for (int k = 0; k < C::STAGES; ++k)
+                if (armed & (1u << k)) mbar_wait(smem_u32(&full[k]), (armed_par >> k) & 1u, p.err, bail, false);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1u, p.err, bail)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&full[s]), ph, p.err, bail)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t ad = desc_sw128(smem_u32(sa + s * C::A_BYTES));
+                    const uint64_t bd = desc_sw128(smem_u32(sb + s * C::B_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16(d, ad + 2 * kk, bd + 2 * kk, C::IDESC, (kb | kk) != 0);
+                    umma_commit(smem_u32(&empty[s]));
+                    if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&tfull[acc]));
+                acc ^= 1;
+                if (!acc) aph ^= 1u;
+            }
+            // every MMA this thread issued has completed before TMEM is freed
+            umma_commit(smem_u32(drain));
+            mbar_wait(smem_u32(drain), 0, p.err, bail, false);
+        }
+    } else {
+        const int q = warp & 3;  // TMEM lane quadrant of this warp
+        const int row = q * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            int u, tm, tn;
+            decode_tile(t, p, u, tm, tn);
+            bool ok = mbar_wait(smem_u32(&tfull[acc]), aph, p.err, bail);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            epilogue_tile<BN>(p, u, tm, tn, row, tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                                      static_cast<uint32_t>(acc * BN));
+            tc_fence_before();
+            mbar_arrive(smem_u32(&tempty[acc]));
+            acc ^= 1;
+            if (!acc) aph ^= 1u;
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int BN>
+cudaError_t launch_gemm_bn(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p0, cudaStream_t st) {
+    using C = GemmCfg<BN>;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    GemmParams p = p0;
+    p.tiles_m = (p.M + BM - 1) / BM;
+    p.tiles_n = (p.N + BN - 1) / BN;
+    p.num_kb = (p.K + BK - 1) / BK;
+    const int total = p.units * p.tiles_m * p.tiles_n;
+    if (total == 0) return cudaSuccess;
+    const int grid = total < device_sm_count() ? total : device_sm_count();
+    ns_gemm_kernel<BN><<<grid, kGemmThreads, C::SMEM, st>>>(tma, tmb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ns_norm(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
+                           const uint16_t* u_stage, char* ws, float eps, cudaStream_t st) {
+    float* partials = reinterpret_cast<float*>(ws + c.part_off);
+    float* inv = reinterpret_cast<float*>(ws + c.inv_off);
+    dim3 g1(c.parts, c.n_units);
+    ns_norm_partial_kernel<<<g1, 256, 0, st>>>(units_dev, u_root, u_stage, partials, c.parts, c.part_len);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ns_norm_final_kernel<<<(c.n_units + 7) / 8, 256, 0, st>>>(partials, c.parts, inv, eps, c.n_units);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
+                              const uint16_t* u_stage, char* ws, cudaStream_t st) {
+    dim3 g(c.np / 64, c.mp / 64, c.n_units);
+    ns_prepare_kernel<<<g, 256, 0, st>>>(units_dev, u_root, u_stage, reinterpret_cast<const float*>(ws + c.inv_off),
+                                         reinterpret_cast<uint16_t*>(ws + c.x_off[0]),
+                                         reinterpret_cast<uint16_t*>(ws + c.xt_off[0]), c.m, c.n, c.mp, c.np);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ns_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p, int bn,
+                           cudaStream_t st) {
+    return bn == 256 ? launch_gemm_bn<256>(tma, tmb, p, st) : launch_gemm_bn<128>(tma, tmb, p, st);
+}
+
+}  // namespace hm

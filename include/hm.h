@@ -1,0 +1,252 @@
+/*
+ * hm.h -- C ABI of the GB300 update-phase library (libhm).
+ *
+ * Implements the update phase of "SS-HSDP: Efficient and Flexible Sharded
+ * Data Parallelism via Runtime-Update Decoupling" on one GPU:
+ *   f0  momentum            (section 3.1 example EG1; Figure 4 "Local momentum")
+ *   P2P fragment gather     (section 3.2 "Distributed updates"; section 3.4)
+ *   f1  batched Newton-Schulz (EG1; section 4.1 "Batched Update and Transform")
+ *   P2P return + f2 update  (EG1; section 3.4; Figure 4 "Local main-weight update")
+ *   G   MXFP8 requant       (EG1; Figure 4 "K-major scale layout", "UE8M0")
+ * plus the elementwise AdamW update (section 5.2) and the data-tree / shard-
+ * chain metadata the update is planned from (section 3.2, section 4.2).
+ *
+ * The ZeRO ranks are emulated: every field (w, m, g, u, v, q, s) is ONE device
+ * allocation holding `so` rank segments in rank order, each starting on a
+ * multiple of HM_SEG_ALIGN elements with HM_SEG_GAP canary elements before,
+ * between and after them.  The point-to-point exchange of the paper becomes an
+ * in-HBM gather / scatter between segments.
+ *
+ * Conventions for every call:
+ *   - Return value: HM_OK (0) or a negative hm_status; hm_status_str() names it.
+ *   - Device pointers are caller-owned (e.g. allocated by PyTorch); the
+ *     library never frees them.  Handles (hm_tree, hm_chain, hm_muon_plan) are
+ *     host metadata owned by the library and released by their *_destroy call.
+ *   - Geometry, alignment, overlap and unit checks run on the host before any
+ *     launch; a failing check launches nothing and returns its status.
+ *   - Launches are asynchronous on the given stream (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  A launch error is returned as
+ *     HM_ERR_CUDA.  Device-side wait timeouts are recorded in a device error
+ *     word that hm_device_error() reads.
+ *   - Element offsets and lengths are int64 element counts, not bytes, unless
+ *     a name says _bytes.
+ */
+#ifndef HM_H
+#define HM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int hm_status;
+#define HM_OK             0
+#define HM_ERR_ARG       -1   /* null pointer, bad enum, negative size          */
+#define HM_ERR_GEOMETRY  -2   /* view or range outside its parent / list        */
+#define HM_ERR_OVERLAP   -3   /* storage overlap where disjointness is required */
+#define HM_ERR_ALIGN     -4   /* offset / length not aligned as required        */
+#define HM_ERR_DTYPE     -5   /* unsupported dtype for the call                 */
+#define HM_ERR_UNITS     -6   /* units do not tile the tensor list              */
+#define HM_ERR_CUDA      -7   /* a CUDA runtime / driver call failed            */
+#define HM_ERR_ARCH      -8   /* device is not sm_103 (GB300)                   */
+#define HM_ERR_TIMEOUT   -9   /* a device-side wait gave up (see hm_device_error) */
+#define HM_ERR_WORKSPACE -10  /* workspace too small or not the uploaded one    */
+#define HM_ERR_STATE     -11  /* call out of order (e.g. plan not uploaded)     */
+
+typedef enum { HM_U8 = 0, HM_BF16 = 1, HM_F32 = 2, HM_E4M3 = 3 } hm_dtype;
+
+#define HM_SEG_ALIGN 1024   /* elements */
+#define HM_SEG_GAP   1024   /* elements */
+#define HM_MX_BLOCK  32     /* elements per MXFP8 scale */
+
+/* Name of a status code (static string). */
+const char* hm_status_str(hm_status s);
+
+/* Reads and clears the device error word of the current device.  *code = 0
+ * when no kernel recorded an error; otherwise the first recorded code (a
+ * device-side wait that gave up, HM_ERR_TIMEOUT).  Synchronises the device. */
+hm_status hm_device_error(int* code);
+
+/* ------------------------------------------------------------------------ */
+/* Data tree (section 3.2 "Data Tree"): a root node owns one allocation; every
+ * other node is a view (parent, byte offset, dtype, shape) and reaches the
+ * storage through its accumulated offset. */
+typedef struct hm_tree hm_tree;
+
+/* root: device (or host) address of the allocation, NOT owned by the tree;
+ * root_bytes > 0.  Node 0 is the root (dtype HM_U8, shape [root_bytes]). */
+hm_status create_data_tree(hm_tree** out, void* root, size_t root_bytes);
+
+/* Adds a view of `parent`.  Rejects (HM_ERR_GEOMETRY) a view extending past its
+ * parent, (HM_ERR_ALIGN) an accumulated offset not a multiple of the element
+ * size, (HM_ERR_ARG) ndim outside 1..8 or a negative extent. */
+hm_status data_tree_add_view(hm_tree* t, int parent, size_t byte_off, hm_dtype dtype,
+                             int ndim, const int64_t* shape, int* node_out);
+
+/* Address (root + accumulated offset) and accumulated offset of a node. */
+hm_status data_tree_resolve(const hm_tree* t, int node, void** ptr, size_t* root_off);
+
+/* HM_ERR_OVERLAP if any two of the given nodes share a byte, else HM_OK. */
+hm_status data_tree_check_disjoint(const hm_tree* t, const int* nodes, int n);
+
+void tree_destroy(hm_tree* t);
+
+/* ------------------------------------------------------------------------ */
+/* Shard chain (section 3.2 "Shard Chain"; section 4.2 "Fully Zero Copy").
+ * A tensor list of n elements is cut at ZeRO-1 edges E_0..E_so (default
+ * E_c = 32*floor(c*n/(32*so)); n must be a multiple of 32).  z1 chunk
+ * c = i*(so/sw) + j is owned by rank i + j*sw (owners [0,2,1,3] for so = 4,
+ * sw = 2).  A level of degree s (sw for z3, sg for z2) has chunk k = z1 chunks
+ * [k*so/s, (k+1)*so/s).  Degrees must nest: sw | sg | so. */
+typedef struct hm_chain hm_chain;
+
+typedef struct {
+    int32_t chunk;        /* chunk index at the requested level            */
+    int32_t rank;         /* z1: owning rank; z2/z3: lowest rank holding it */
+    int64_t seg_offset;   /* element offset inside that chunk              */
+    int64_t unit_offset;  /* element offset inside the queried range       */
+    int64_t length;       /* elements                                      */
+    int64_t root_offset;  /* z1 only: element offset in the emulated root  */
+} hm_fragment;
+
+/* z1_edges: NULL for the default edges, else so+1 non-decreasing multiples of
+ * 32 from 0 to n.  edge_shift (only with z1_edges == NULL): NULL, or so+1
+ * multiples of 32 added to the default edges (ragged edges; entries 0 and so
+ * must be 0).  Rejects unaligned edges or shifts (HM_ERR_ALIGN), edges that
+ * decrease or miss 0 / n (HM_ERR_GEOMETRY), degrees that do not nest
+ * (HM_ERR_GEOMETRY), n not a multiple of 32 (HM_ERR_ALIGN). */
+hm_status shard_chain(hm_chain** out, int64_t n, int so, int sw, int sg, const int64_t* z1_edges,
+                      const int64_t* edge_shift);
+
+/* Emulated root layout: *total = elements of one field allocation; bases[r]
+ * (so entries, may be NULL) = element offset of rank r's segment; lens[r] =
+ * its length; chunk_of_rank[r] = its z1 chunk. */
+hm_status shard_chain_layout(const hm_chain* c, int64_t* total, int64_t* bases, int64_t* lens,
+                             int32_t* chunk_of_rank);
+
+/* Fragments of the logical range [a, b) at level 1 (z1), 2 (z2) or 3 (z3), in
+ * range order.  Writes min(cap, count) entries, *n = count. */
+hm_status shard_chain_fragments(const hm_chain* c, int64_t a, int64_t b, int level,
+                                hm_fragment* out, int cap, int* n);
+
+/* Adds one view per rank segment (dtype, shape [len_r]) as children of node 0
+ * of a field's data tree whose root holds the emulated layout; node ids are
+ * written to nodes_out[so]. */
+hm_status shard_chain_segment_views(const hm_chain* c, hm_tree* t, hm_dtype dtype, int* nodes_out);
+
+void chain_destroy(hm_chain* c);
+
+/* ------------------------------------------------------------------------ */
+/* Muon update of a tensor list (EG1; section 3.4 "Update"; section 4.1). */
+typedef struct {
+    int64_t offset;   /* element offset of the unit in the tensor list   */
+    int32_t rows;     /* a unit is a contiguous rows x cols row-major block */
+    int32_t cols;
+} hm_unit_desc;
+
+typedef struct hm_muon_plan hm_muon_plan;
+
+/* Plans the update of the units (sorted, disjoint, tiling [0, n) exactly:
+ * else HM_ERR_UNITS; rows*cols a multiple of 32 and cols <= 65535: else
+ * HM_ERR_ALIGN / HM_ERR_GEOMETRY).  Classifies each unit as local (one z1
+ * fragment) or straddling, picks its execution rank (owner of its first
+ * element), groups units by Newton-Schulz shape class (min, max of rows,
+ * cols) and lays out the workspace.  Host only. */
+hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const hm_unit_desc* units, int n_units);
+
+typedef struct {
+    int32_t n_units, n_local, n_straddling, n_classes;
+    int64_t staging_elems;    /* elements of the u / v staging of straddling units */
+    int64_t workspace_bytes;  /* device workspace muon_update_units needs      */
+    int32_t n_fragments;      /* z1 fragments of straddling units               */
+} hm_muon_plan_info;
+hm_status muon_plan_query(const hm_muon_plan* p, hm_muon_plan_info* info);
+
+/* Per-unit plan facts: *exec_rank, *n_frags, *cls (shape class), *local. */
+hm_status muon_plan_unit(const hm_muon_plan* p, int unit, int32_t* exec_rank, int32_t* n_frags,
+                         int32_t* cls, int32_t* local);
+
+/* Copies the plan's device tables into `workspace` (device, >= workspace_bytes,
+ * 1024-byte aligned) and encodes the tensor maps of its scratch regions.  Must
+ * precede muon_update_units with that workspace; calling it again with another
+ * workspace re-targets the plan.  Needs a current sm_103 device. */
+hm_status muon_plan_upload(hm_muon_plan* p, void* workspace, size_t workspace_bytes, void* stream);
+
+typedef struct {
+    float lr;            /* 0.02 */
+    float momentum;      /* mu, 0.95 */
+    float weight_decay;  /* decoupled, applied in f2 when != 0 */
+    float eps;           /* Newton-Schulz normalisation, 1e-7 */
+    float ns_a, ns_b, ns_c;   /* 3.4445, -4.7750, 2.0315 */
+    int32_t ns_steps;    /* 5 */
+    int32_t nesterov;    /* 0: u = bf16(m); 1: u = bf16(g + mu*m) */
+    int32_t alpha_mode;  /* 0: 1; 1: sqrt(max(1, rows/cols)); 2: 0.2*sqrt(max(rows, cols)) */
+} hm_muon_hparams;
+
+typedef struct {  /* device roots, each in the chain's emulated layout */
+    float*    w;   /* fp32 main weight,     total elements         */
+    float*    m;   /* fp32 momentum                                  */
+    const float* g;/* fp32 main gradient                             */
+    uint16_t* u;   /* bf16 intermediate u (bit patterns)             */
+    float*    v;   /* fp32 update direction v                        */
+    uint8_t*  q;   /* E4M3 runtime weight, same element offsets as w */
+    uint8_t*  s;   /* UE8M0 scales, element offset / 32              */
+} hm_muon_bufs;
+
+#define HM_STAGE_F0      1   /* m <- mu m + g; u = bf16(m)                 */
+#define HM_STAGE_GATHER  2   /* u fragments of straddling units -> staging  */
+#define HM_STAGE_NS      4   /* f1 for every unit -> v                      */
+#define HM_STAGE_F2      8   /* v fragments -> owners; w <- w - lr alpha v  */
+#define HM_STAGE_REQUANT 16  /* G: w -> (q, s) in every segment             */
+#define HM_STAGE_ALL     31
+
+/* Runs the selected stages, in the order above, on `stream`.  u and v of
+ * straddling units live in the workspace staging; v of local units is
+ * written to the v root at the unit's own offsets. */
+hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs* bufs,
+                            const hm_muon_hparams* hp, void* workspace, size_t workspace_bytes,
+                            int stages, void* stream);
+
+/* Device address of a straddling unit's u / v staging (after upload). */
+hm_status muon_plan_staging(const hm_muon_plan* p, int unit, uint16_t** u_stage, float** v_stage);
+
+void muon_plan_destroy(hm_muon_plan* p);
+
+/* ------------------------------------------------------------------------ */
+/* Fused elementwise AdamW over one flat shard (section 5.2; PyTorch AdamW
+ * semantics: decoupled weight decay, bias correction with step t >= 1).
+ * w, m, v: fp32 [n]; g: [n] of g_dtype (HM_BF16 or HM_F32).  n = 0 is a no-op.
+ * Pointers must be 16-byte aligned (HM_ERR_ALIGN). */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+    int32_t step;
+} hm_adamw_hparams;
+
+hm_status adamw_update_flat(float* w, const void* g, hm_dtype g_dtype, float* m, float* v,
+                            int64_t n, const hm_adamw_hparams* hp, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* G: MXFP8 requantization (EG1; OCP MX format): for every 1 x 32 block along K
+ * of each [rows][K] fp32 tensor, e = clamp(floor(log2 amax) - 8, -127, 127),
+ * scale code e + 127, elements E4M3 = RNE(x * 2^-e) saturated to +-448.
+ * Codes are written at dst_offset (same [rows][K] layout: the packed QKV /
+ * grouped-GEMM layout of the source), scales as [rows][K/32] at
+ * scale_offset.  K must be a multiple of 32; src_offset and dst_offset
+ * multiples of 32 (HM_ERR_ALIGN).  n = 0 is a no-op. */
+typedef struct {
+    int64_t src_offset;    /* elements of w     */
+    int64_t dst_offset;    /* elements of q     */
+    int64_t scale_offset;  /* elements of s     */
+    int64_t rows;
+    int64_t k;
+} hm_mx_tensor;
+
+hm_status mxfp8_requant_packed(const float* w, uint8_t* q, uint8_t* scales,
+                               const hm_mx_tensor* tensors, int n, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HM_H */

@@ -15,7 +15,8 @@ group-rank order, owners [0, 2, 1, 3] for so = 4, sw = sg = 2.
 
 Readings where the paper is silent (listed in the design notes):
   * edges: E_c = 32 * floor(c * N / (32 * so)), c = 0..so (32-aligned, nearly
-    even, not unit-aligned); N must be a multiple of 32;
+    even, not unit-aligned); N must be a multiple of 32; a workload may move
+    the interior edges by a given 32-aligned shift (ragged edges);
   * owner of z1 chunk c = i*R + j (R = so/sw) is rank i + j*sw;
   * a level of degree s has chunk k = z1 chunks [k*so/s, (k+1)*so/s);
   * execution rank of a unit = owner of the chunk holding its first element
@@ -88,10 +89,19 @@ class DataTree:
 # ----------------------------------------------------------------------------
 # Shard chain
 # ----------------------------------------------------------------------------
-def z1_edges(n: int, so: int) -> List[int]:
+def z1_edges(n: int, so: int, shift: Sequence[int] = None) -> List[int]:
+    """Default ZeRO-1 edges, optionally moved by a ragged 32-aligned shift
+    (shift[0] = shift[so] = 0)."""
     if n % 32:
         raise ValueError("tensor-list length must be a multiple of 32")
-    return [32 * ((c * n) // (32 * so)) for c in range(so + 1)]
+    e = [32 * ((c * n) // (32 * so)) for c in range(so + 1)]
+    if shift is not None:
+        if shift[0] or shift[so] or any(x % 32 for x in shift):
+            raise ValueError("edge shift must be 32-aligned and keep 0 and n")
+        e = [a + b for a, b in zip(e, shift)]
+        if any(b < a for a, b in zip(e[:-1], e[1:])):
+            raise ValueError("shifted edges decrease")
+    return e
 
 
 def owner(c: int, so: int, sw: int) -> int:

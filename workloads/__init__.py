@@ -85,6 +85,7 @@ class Config:
     so: int                      # ZeRO-1 sharding degree (emulated ranks)
     sw: int                      # ZeRO-3 degree
     sg: int                      # ZeRO-2 degree
+    edge_shift: Optional[List[int]] = None   # ragged ZeRO-1 edges: per-edge 32-aligned shift
     w_std: float = 0.02
     g_std: float = 1e-3
     seed: int = 0
@@ -152,6 +153,17 @@ def lm_layer() -> Config:
                   "8 emulated ranks", "muon", b.members, b.units, so=8, sw=4, sg=4)
 
 
+def ragged_shift(so: int, max_blocks: int, seed: int) -> List[int]:
+    """A seeded ragged-edge shift: interior edges move by a nonzero multiple of
+    32 elements, at most max_blocks * 32 either way; the end edges stay."""
+    rng = np.random.default_rng(seed)
+    mag = rng.integers(1, max_blocks + 1, so + 1)
+    sign = np.where(rng.integers(0, 2, so + 1) == 0, -1, 1)
+    sh = [int(32 * m * s) for m, s in zip(mag, sign)]
+    sh[0] = sh[so] = 0
+    return sh
+
+
 def moe_layer() -> Config:
     b = _ListBuilder()
     for e in range(64):
@@ -160,9 +172,12 @@ def moe_layer() -> Config:
         b.add(f"up{e}", 1408, 2048)
     for e in range(64):
         b.add(f"down{e}", 2048, 1408)
+    # even edges would fall exactly on expert boundaries (12 matrices per rank);
+    # ragged edges make every one of the 15 interior edges split a matrix
     return Config("moe_layer", "64 experts, gate/up [1408][2048], down [2048][1408]; "
-                  "192 expert-matrix Muon units; 16 emulated ranks",
-                  "muon", b.members, b.units, so=16, sw=8, sg=8)
+                  "192 expert-matrix Muon units; 16 emulated ranks with ragged edges",
+                  "muon", b.members, b.units, so=16, sw=8, sg=8,
+                  edge_shift=ragged_shift(16, 2048, seed=16))
 
 
 def video_dit(layers: int = 8) -> Config:
