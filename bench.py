@@ -1,0 +1,430 @@
+"""Benchmark of the update phase (SS-HSDP: f0 momentum, fragment gather,
+batched Newton-Schulz, scatter + f2, MXFP8 requant) on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one call of muon_update_units over the whole workload (all five
+stages), inputs resident in HBM.  Prints one JSON line on rank 0.  Under
+torchrun each rank runs an independent replica on its own GPU (the path has
+no cross-GPU exchange on one box): whole-job params/s = ranks * P * K / max
+over ranks of the timed region.
+
+--impl reference times the CPU oracle (plain NumPy) on the host cores on a
+bounded sample of the same workload, scaled to params/s.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "update-phase params/sec; NS TFLOP/s and requant GB/s as % of GB300 peak"
+UNIT = "params/s"
+
+
+def ns_flops(cfg, steps: int) -> float:
+    """Algorithmic Newton-Schulz FLOP of one update: per unit and iteration
+    4 m^2 n (X X^T and B X) + 2 m^3 (A A), m = min, n = max of its shape."""
+    tot = 0.0
+    for u in cfg.units:
+        m, n = min(u.rows, u.cols), max(u.rows, u.cols)
+        tot += steps * (4.0 * m * m * n + 2.0 * m ** 3)
+    return tot
+
+
+def straddling_elems(cfg, plan_info) -> int:
+    return int(plan_info.staging_elems)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sustained": d["bf16_tflops_sustained"],
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in self.rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        pw = [num(r[3]) for r in self.rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows), "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle on a bounded sample (cpu_baseline and --impl reference)
+# ----------------------------------------------------------------------------
+def oracle_sample_step(cfg, rng_seed: int = 0):
+    """One pass of the oracle over a bounded sample of the workload; returns
+    (seconds, extrapolated seconds for the whole workload, description).
+
+    Sample: every stage on a 262,144-element slice (f0, f2, MXFP8 requant;
+    gather is a copy), Newton-Schulz in full for one unit of the smallest
+    shape class, and for every larger class one product of each of the three
+    kinds on an m x m slice; the class's time is extrapolated by its
+    algorithmic FLOP."""
+    from oracle import muon as OM
+    from oracle import mxfp8 as OX
+    rng = np.random.default_rng(rng_seed)
+    t_start = time.perf_counter()
+    n_el = 1 << 18
+    w = (rng.standard_normal(n_el) * 0.02).astype(np.float32)
+    g = (rng.standard_normal(n_el) * 1e-3).astype(np.float32)
+    m = np.zeros(n_el, np.float32)
+    t0 = time.perf_counter()
+    m, u = OM.momentum(m, g, 0.95)
+    v = OM.bf16_bits_to_f32(u)
+    w = OM.main_weight_update(w, v, 0.02, 1.0)
+    OX.requant_list(w, [(0, n_el // 4096, 4096)])
+    t_elem = (time.perf_counter() - t0) / n_el
+    h = cfg.muon
+    classes = {}
+    for un in cfg.units:
+        key = (min(un.rows, un.cols), max(un.rows, un.cols))
+        classes[key] = classes.get(key, 0) + 1
+    t_ns = 0.0
+    for (mm, nn), cnt in sorted(classes.items()):
+        if mm <= 256:
+            x = rng.standard_normal((mm, nn)).astype(np.float32) * np.float32(1e-3)
+            t0 = time.perf_counter()
+            OM.newton_schulz(x, h.ns_steps, h.ns_a, h.ns_b, h.ns_c, h.eps)
+            t_ns += (time.perf_counter() - t0) * cnt
+        else:
+            x = rng.standard_normal((mm, mm)).astype(np.float32) * np.float32(1e-3)
+            t0 = time.perf_counter()
+            A = x @ x.T
+            B = np.float32(h.ns_b) * A + np.float32(h.ns_c) * (A @ A)
+            _ = np.float32(h.ns_a) * x + B @ x
+            dt = time.perf_counter() - t0
+            sample_flops = 6.0 * mm ** 3
+            class_flops = cnt * h.ns_steps * (4.0 * mm * mm * nn + 2.0 * mm ** 3)
+            t_ns += dt * class_flops / sample_flops
+    total = t_elem * cfg.numel + t_ns
+    desc = ("oracle f0+f2+MXFP8 on 262144 elements, full Newton-Schulz on one unit per small class, one "
+            "X X^T / A A / B X triple on an m x m slice per large class; extrapolated by elements and FLOP")
+    return time.perf_counter() - t_start, total, desc
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, cfg):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample_step(cfg)
+    times, totals = [], []
+    desc = ""
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        dt, total, desc = oracle_sample_step(cfg, rng_seed=k)
+        times.append(dt)
+        totals.append(total)
+    wall = time.perf_counter() - t0
+    per_step = statistics.median(totals)
+    value = cfg.numel / per_step
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": cfg.name, "params": cfg.numel, "units": len(cfg.units)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": desc, "sample_wall_s": wall},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, cfg):
+    import torch
+
+    from head_muon_mxfp8_gb300 import abi
+    from head_muon_mxfp8_gb300.session import MuonSession, muon_hparams
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    abi.lib()
+
+    sess = MuonSession.from_config(cfg, device=dev, canaries=False)
+    data = workloads.generate_device(cfg, dev, seed=cfg.seed + rank)
+    sess.load("w", data["w"])
+    sess.load("g", data["g"])
+    sess.m.zero_()
+    del data
+    hp = muon_hparams(cfg.muon)
+    stream = torch.cuda.Stream(device=dev)
+    info = sess.info
+    launches_per_step = (1 + (1 if info.n_straddling else 0) + info.n_classes * (3 + 3 * cfg.muon.ns_steps) + 2)
+
+    def step(ev=None):
+        if ev is None:
+            sess.run(hp, abi.HM_STAGE_ALL, stream)
+            return
+        ev[0].record(stream)
+        sess.run(hp, abi.HM_STAGE_F0 | abi.HM_STAGE_GATHER, stream)
+        ev[1].record(stream)
+        sess.run(hp, abi.HM_STAGE_NS, stream)
+        ev[2].record(stream)
+        sess.run(hp, abi.HM_STAGE_F2, stream)
+        ev[3].record(stream)
+        sess.run(hp, abi.HM_STAGE_REQUANT, stream)
+        ev[4].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    if abi.hm_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks.stop()
+    ms = t_begin.elapsed_time(t_end)
+    stage_ms = {"f0_gather": [], "ns": [], "f2": [], "requant": []}
+    for e in evs:
+        stage_ms["f0_gather"].append(e[0].elapsed_time(e[1]))
+        stage_ms["ns"].append(e[1].elapsed_time(e[2]))
+        stage_ms["f2"].append(e[2].elapsed_time(e[3]))
+        stage_ms["requant"].append(e[3].elapsed_time(e[4]))
+    stage_ms = {k: statistics.mean(v) for k, v in stage_ms.items()}
+    if abi.hm_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * cfg.numel * args.steps / (ms / 1e3)
+
+    # ---- end to end: host gradient in, host MXFP8 runtime weight out -----
+    e2e_steps = max(1, min(3, args.steps))
+    g_host = torch.empty(sess.total, dtype=torch.float32, pin_memory=True)
+    g_host.copy_(sess.g, non_blocking=False)
+    q_host = torch.empty(sess.total, dtype=torch.uint8, pin_memory=True)
+    s_host = torch.empty(sess.total // 32, dtype=torch.uint8, pin_memory=True)
+    with torch.cuda.stream(stream):
+        for k in range(e2e_steps + 1):
+            if k == 1:
+                torch.cuda.synchronize()
+                if dist:
+                    dist.barrier()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            sess.g.copy_(g_host, non_blocking=True)
+            sess.run(hp, abi.HM_STAGE_ALL, stream)
+            q_host.copy_(sess.q, non_blocking=True)
+            s_host.copy_(sess.s, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * cfg.numel * e2e_steps / (e2e_ms / 1e3)
+    h2d = sess.total * 4
+    d2h = sess.total + sess.total // 32
+
+    # ---- AdamW on the flat 64M shard (its own small timed loop) ----------
+    adamw = None
+    if not args.skip_adamw:
+        adamw = bench_adamw(dev, stream)
+
+    peaks = load_peaks()
+    flops = ns_flops(cfg, cfg.muon.ns_steps)
+    ns_tflops = flops / (stage_ms["ns"] / 1e3) / 1e12
+    P = cfg.numel
+    strad = straddling_elems(cfg, info)
+    bytes_f0 = 14.0 * P + 4.0 * strad
+    bytes_f2 = 12.0 * P
+    bytes_rq = 5.03125 * P
+    kern = {
+        "f0_gather": {"gbs": bytes_f0 / (stage_ms["f0_gather"] / 1e3) / 1e9},
+        "f2_scatter": {"gbs": bytes_f2 / (stage_ms["f2"] / 1e3) / 1e9},
+        "mxfp8_requant": {"gbs": bytes_rq / (stage_ms["requant"] / 1e3) / 1e9},
+    }
+    for k in kern:
+        kern[k]["frac"] = kern[k]["gbs"] / peaks["hbm_gbs"]
+    if adamw:
+        kern["adamw_flat_64M"] = adamw
+        adamw["frac"] = adamw["gbs"] / peaks["hbm_gbs"]
+    roofline = {"bound": "tensor", "achieved": ns_tflops, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                "frac": ns_tflops / peaks["bf16_sustained"], "traffic": None,
+                "kernel": "Newton-Schulz stage (ns_gemm_kernel, 15 launches per shape class, plus norm/prepare)",
+                "peak_kind": f"bf16 dense sustained ({peaks['source']})",
+                "frac_of_burst": ns_tflops / peaks["bf16"]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        t0 = time.perf_counter()
+        _, total, desc = oracle_sample_step(cfg)
+        cpu = {"value": cfg.numel / total, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+               "sample": desc, "sample_wall_s": time.perf_counter() - t0}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16+fp32", "data": "synthetic (seeded N(0,0.02) w, N(0,1e-3) g)",
+                "config": {"workload": f"{cfg.name}: {cfg.description}", "params": P, "units": len(cfg.units),
+                           "shape_classes": info.n_classes, "straddling_units": info.n_straddling,
+                           "emulated_ranks": cfg.so, "parallelism": f"replica x{world}",
+                           "l2": "inputs larger than L2 (resident state ~%.0f GB)" % (
+                               (sess.total * 21 + sess.ws_bytes) / 1e9)},
+                "ns_tflops": ns_tflops, "ns_flops_per_step": flops, "stages_ms": stage_ms, "kernels": kern,
+                "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                        "steps": e2e_steps},
+                "gpu_launches": launches_per_step * args.steps, "clocks": clocks.summary()}
+        print(json.dumps(line), flush=True)
+    sess.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def bench_adamw(dev, stream, steps: int = 10):
+    import torch
+
+    from head_muon_mxfp8_gb300 import abi
+    from head_muon_mxfp8_gb300.session import adamw_hparams
+    cfg = workloads.flat_adamw()
+    n = cfg.numel
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    w = torch.empty(n, device=dev).normal_(0, 0.02, generator=gen)
+    g = torch.empty(n, device=dev).normal_(0, 1e-3, generator=gen).to(torch.bfloat16)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    hp = adamw_hparams(cfg.adamw, 1)
+    sh = int(stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            abi.adamw_update_flat(w.data_ptr(), g.data_ptr(), abi.HM_BF16, m.data_ptr(), v.data_ptr(), n, hp, sh)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            abi.adamw_update_flat(w.data_ptr(), g.data_ptr(), abi.HM_BF16, m.data_ptr(), v.data_ptr(), n, hp, sh)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"gbs": 26.0 * n / (ms / 1e3) / 1e9, "ms": ms, "bytes_per_elem": 26,
+            "workload": "flat_adamw 67,108,864 fp32 params, bf16 grads (inputs larger than L2)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="video_dit", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-adamw", action="store_true")
+    args = ap.parse_args()
+    cfg = workloads.get(args.workload)
+    if cfg.optimizer != "muon":
+        raise SystemExit("bench workloads are Muon tensor lists")
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,223 @@
+"""GPU parity of every update-phase kernel against the oracle, through the
+C ABI, at sizes the oracle finishes in seconds (several tiles, ragged
+edges, padded Gram sizes, transposed units, a ragged AdamW tail)."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads  # noqa: E402
+from oracle import adamw as OA  # noqa: E402
+from oracle import muon as OM  # noqa: E402
+from oracle import mxfp8 as OX  # noqa: E402
+
+from muon_parity import check_f0, check_f2, check_ns, check_requant, check_staging  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(hm):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def _session(cfg, dev):
+    from head_muon_mxfp8_gb300.session import MuonSession
+    return MuonSession.from_config(cfg, device=dev)
+
+
+def _hp(h):
+    from head_muon_mxfp8_gb300.session import muon_hparams
+    return muon_hparams(h)
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_ragged", "mixed"])
+def test_muon_update_stage_by_stage(hm, dev, name):
+    cfg = workloads.get(name)
+    data = workloads.generate(cfg, seed=11)
+    s = _session(cfg, dev)
+    m0 = np.zeros_like(data["w"])
+    s.load("w", data["w"])
+    s.load("g", data["g"])
+    s.load("m", m0)
+    hp = _hp(cfg.muon)
+    s.run(hp, hm.HM_STAGE_F0 | hm.HM_STAGE_GATHER)
+    torch.cuda.synchronize()
+    m1 = s.fetch("m").numpy()
+    u1 = s.fetch("u").numpy().view(np.uint16)
+    check_f0(m0, data["g"], m1, u1, cfg.muon.momentum)
+    n_strad = check_staging(s, cfg, u1)
+    assert n_strad == s.info.n_straddling
+    s.run(hp, hm.HM_STAGE_NS)
+    torch.cuda.synchronize()
+    v = s.fetch("v").numpy()
+    # v of straddling units lives in the staging; bring it into logical order
+    for i, un in enumerate(cfg.units):
+        if not hm.muon_plan_unit(s.plan, i)["local"]:
+            v[un.offset:un.offset + un.numel] = s.staging(i)[1].cpu().numpy()
+    check_ns(cfg, u1, v, cfg.muon)
+    s.run(hp, hm.HM_STAGE_F2 | hm.HM_STAGE_REQUANT)
+    torch.cuda.synchronize()
+    w1 = s.fetch("w").numpy()
+    check_f2(cfg, data["w"], v, w1, cfg.muon)
+    check_requant(cfg, w1, s.fetch("q").numpy(), s.fetch("s").numpy())
+    assert all(s.canary_intact().values())
+    assert hm.hm_device_error() == 0
+    s.close()
+
+
+def test_muon_two_steps_all_stages(hm, dev):
+    """Two whole update phases (one call each); momentum carries over."""
+    cfg = workloads.get("mixed")
+    data = workloads.generate(cfg, seed=12)
+    g2 = workloads.gaussian(cfg.numel, cfg.g_std, seed=13)
+    s = _session(cfg, dev)
+    s.load("w", data["w"])
+    s.load("m", np.zeros_like(data["w"]))
+    hp = _hp(cfg.muon)
+    w_prev, m_prev = data["w"], np.zeros_like(data["w"])
+    for g in (data["g"], g2):
+        s.load("g", g)
+        s.run(hp)
+        torch.cuda.synchronize()
+        m = s.fetch("m").numpy()
+        u = s.fetch("u").numpy().view(np.uint16)
+        check_f0(m_prev, g, m, u, cfg.muon.momentum)
+        w = s.fetch("w").numpy()
+        # direction recovered from the f2 result is checked through w itself:
+        # w_prev - w = lr * v elementwise, so compare lr*v with the oracle
+        v = s.fetch("v").numpy()
+        for i, un in enumerate(cfg.units):
+            if not hm.muon_plan_unit(s.plan, i)["local"]:
+                v[un.offset:un.offset + un.numel] = s.staging(i)[1].cpu().numpy()
+        check_ns(cfg, u, v, cfg.muon)
+        check_f2(cfg, w_prev, v, w, cfg.muon)
+        check_requant(cfg, w, s.fetch("q").numpy(), s.fetch("s").numpy())
+        w_prev, m_prev = w, m
+    assert all(s.canary_intact().values())
+    s.close()
+
+
+def test_muon_variants_nesterov_decay_alpha(hm, dev):
+    cfg = workloads.get("mixed")
+    cfg.muon = dataclasses.replace(cfg.muon, nesterov=True, weight_decay=0.1, alpha_mode=1,
+                                   lr=float(np.float32(0.02)))
+    data = workloads.generate(cfg, seed=14)
+    s = _session(cfg, dev)
+    s.load("w", data["w"])
+    s.load("g", data["g"])
+    m0 = workloads.gaussian(cfg.numel, 1e-3, seed=15)
+    s.load("m", m0)
+    s.run(_hp(cfg.muon))
+    torch.cuda.synchronize()
+    m = s.fetch("m").numpy()
+    u = s.fetch("u").numpy().view(np.uint16)
+    check_f0(m0, data["g"], m, u, cfg.muon.momentum, nesterov=True)
+    v = s.fetch("v").numpy()
+    for i, un in enumerate(cfg.units):
+        if not hm.muon_plan_unit(s.plan, i)["local"]:
+            v[un.offset:un.offset + un.numel] = s.staging(i)[1].cpu().numpy()
+    check_ns(cfg, u, v, cfg.muon)
+    check_f2(cfg, data["w"], v, s.fetch("w").numpy(), cfg.muon)
+    s.close()
+
+
+def test_muon_zero_gradient_unit_and_lr_zero(hm, dev):
+    cfg = workloads.get("tiny_ragged")
+    data = workloads.generate(cfg, seed=16)
+    g = data["g"].copy()
+    z = cfg.units[4]
+    g[z.offset:z.offset + z.numel] = 0.0
+    cfg.muon = dataclasses.replace(cfg.muon, lr=0.0)
+    s = _session(cfg, dev)
+    s.load("w", data["w"])
+    s.load("g", g)
+    s.load("m", np.zeros_like(g))
+    s.run(_hp(cfg.muon))
+    torch.cuda.synchronize()
+    v = s.fetch("v").numpy()
+    if hm.muon_plan_unit(s.plan, 4)["local"]:
+        assert (v[z.offset:z.offset + z.numel] == 0).all()
+    w = s.fetch("w").numpy()
+    assert np.array_equal(w.view(np.uint32), data["w"].view(np.uint32))   # lr = 0: w unchanged
+    check_requant(cfg, w, s.fetch("q").numpy(), s.fetch("s").numpy())
+    s.close()
+
+
+def test_mxfp8_requant_packed_special_values(hm, dev):
+    rng = np.random.default_rng(21)
+    tensors = [(0, 64, 256), (64 * 256 + 1024, 33, 96), (64 * 256 + 1024 + 33 * 96 + 32, 7, 4096)]
+    n = tensors[-1][0] + 7 * 4096 + 64
+    w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    w[0:32] = 0.0
+    w[32:64] = -0.0
+    w[64:96] = np.float32(1e-40) * rng.standard_normal(32).astype(np.float32)      # subnormal block
+    w[96:128] = np.float32(3e38) * np.sign(rng.standard_normal(32)).astype(np.float32)
+    w[128:160] = np.ldexp(1.0, rng.integers(-140, 127, 32)).astype(np.float32)    # wide dynamic range
+    w[160:192] = (OX.E4M3_TABLE[rng.integers(0, 127, 32)] * 2.0 ** -20).astype(np.float32)
+    mids = ((OX.E4M3_TABLE[:-1] + OX.E4M3_TABLE[1:]) / 2)
+    w[192:192 + 126] = mids.astype(np.float32)            # ties at e = 0 (block max 448 below)
+    w[192 + 126] = 448.0
+    w[192 + 126 + 1:192 + 128] = -mids[:1]
+    wt = torch.from_numpy(w).to(dev)
+    q = torch.full((n,), 0x5A, dtype=torch.uint8, device=dev)
+    sc = torch.full((n // 32 + 64,), 0x5A, dtype=torch.uint8, device=dev)
+    mx = [(o, o, o // 32 + 7, r, k) for (o, r, k) in tensors]
+    hm.mxfp8_requant_packed(wt.data_ptr(), q.data_ptr(), sc.data_ptr(), mx)
+    torch.cuda.synchronize()
+    qn, sn = q.cpu().numpy(), sc.cpu().numpy()
+    for (o, r, k) in tensors:
+        cq, cs = OX.quantize_tensor(w[o:o + r * k].reshape(r, k))
+        assert np.array_equal(qn[o:o + r * k], cq.ravel())
+        assert np.array_equal(sn[o // 32 + 7:o // 32 + 7 + r * k // 32], cs.ravel())
+    assert (qn[64 * 256:64 * 256 + 1024] == 0x5A).all()     # the gap between tensors is untouched
+
+
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_adamw_update_flat(hm, dev, gdt):
+    from head_muon_mxfp8_gb300.session import adamw_hparams
+    h = workloads.AdamWHparams()
+    n = (1 << 20) + 3
+    rng = np.random.default_rng(22)
+    w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    wt, mt, vt = (torch.from_numpy(x.copy()).to(dev) for x in (w, m, v))
+    w64, m64, v64 = w.astype(np.float64), m.astype(np.float64), v.astype(np.float64)
+    for step in (1, 2, 3):
+        g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+        if gdt == "bf16":
+            gb = OM.bf16_rne_bits(g)
+            gt = torch.from_numpy(gb.view(np.int16)).to(dev)
+            gx = OM.bf16_bits_to_f32(gb)
+            code = hm.HM_BF16
+        else:
+            gt = torch.from_numpy(g).to(dev)
+            gx = g
+            code = hm.HM_F32
+        hm.adamw_update_flat(wt.data_ptr(), gt.data_ptr(), code, mt.data_ptr(), vt.data_ptr(), n,
+                             adamw_hparams(h, step))
+        torch.cuda.synchronize()
+        w_in, m_in = w64, m64
+        w64, m64, v64 = OA.adamw_step(w64, gx, m64, v64, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, step)
+        gw, gm, gv = wt.cpu().numpy(), mt.cpu().numpy(), vt.cpu().numpy()
+        # relative error 1e-6 against the magnitudes of the summed terms
+        assert (np.abs(gw - w64) <= 1e-6 * np.maximum(np.abs(w64), np.abs(w_in))).all()
+        assert (np.abs(gm - m64) <= 1e-6 * (np.abs(h.beta1 * m_in) + np.abs((1 - h.beta1) * gx)) + 1e-30).all()
+        assert (np.abs(gv - v64) <= 1e-6 * np.abs(v64) + 1e-30).all()
+        # continue from the GPU state so the next step compares like with like
+        w64, m64, v64 = gw.astype(np.float64), gm.astype(np.float64), gv.astype(np.float64)
+
+
+def test_empty_inputs_are_noops(hm, dev):
+    from head_muon_mxfp8_gb300.session import adamw_hparams
+    hm.adamw_update_flat(0, 0, hm.HM_BF16, 0, 0, 0, adamw_hparams(workloads.AdamWHparams(), 1))
+    hm.mxfp8_requant_packed(0, 0, 0, [])
+    x = torch.zeros(64, device=dev)
+    hm.mxfp8_requant_packed(x.data_ptr(), x.data_ptr(), x.data_ptr(), [(0, 0, 0, 0, 32)])
+    torch.cuda.synchronize()
+    assert hm.hm_device_error() == 0

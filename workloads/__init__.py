@@ -230,3 +230,45 @@ def gaussian(shape, std: float, seed: int) -> np.ndarray:
     """A seeded float32 N(0, std) array."""
     rng = np.random.default_rng(seed)
     return rng.standard_normal(shape, dtype=np.float32) * np.float32(std)
+
+
+def generate_device(cfg: Config, device, seed: Optional[int] = None):
+    """Seeded inputs drawn on the GPU for the full-size workloads (the host
+    generator would take minutes at 2.3 G elements): w ~ N(0, w_std) then
+    g ~ N(0, g_std), float32, from one torch.Generator on `device`.  Tests
+    that compare with the oracle copy the drawn values back."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(cfg.seed if seed is None else seed)
+    n = cfg.numel
+    w = torch.empty(n, dtype=torch.float32, device=device)
+    w.normal_(0.0, cfg.w_std, generator=gen)
+    g = torch.empty(n, dtype=torch.float32, device=device)
+    g.normal_(0.0, cfg.g_std, generator=gen)
+    return {"w": w, "g": g}
+
+
+def mixed() -> Config:
+    """A small config that exercises every path: per-head units, transposed
+    and non-transposed whole matrices, a Gram size that is not a multiple of
+    128, a width that is not a multiple of 64, and ragged edges over 8 ranks."""
+    b = _ListBuilder()
+    _qkv(b, "", d=512, hq=4, hkv=4, dh=64)       # 12 x (64 x 512)
+    b.add("up", 1536, 512)                       # transposed, 512 x 1536
+    b.add("down", 512, 1536)                     # 512 x 1536
+    for e in range(3):
+        b.add(f"e{e}", 192, 320)                 # m = 192 -> padded to 256
+    b.add("odd", 96, 160)                        # n = 160 -> padded to 192
+    return Config("mixed", "test mix of unit shapes over 8 ragged ranks", "muon", b.members, b.units,
+                  so=8, sw=4, sg=4, edge_shift=ragged_shift(8, 400, seed=8))
+
+
+def tiny_ragged() -> Config:
+    cfg = tiny()
+    cfg.name = "tiny_ragged"
+    cfg.edge_shift = ragged_shift(4, 200, seed=4)
+    return cfg
+
+
+CONFIGS["mixed"] = mixed
+CONFIGS["tiny_ragged"] = tiny_ragged
