@@ -47,7 +47,7 @@ def check_ns(cfg, u_bits, v_gpu, hp, units=None, tol=NS_TOL):
         sl = slice(un.offset, un.offset + un.numel)
         ref = OM.newton_schulz(u32[sl].reshape(un.rows, un.cols), hp.ns_steps, hp.ns_a, hp.ns_b, hp.ns_c, hp.eps)
         nrm = np.linalg.norm(ref)
-        err = np.linalg.norm(v_gpu[sl].astype(np.float64) - ref) / nrm if nrm > 0 else np.abs(v_gpu[sl]).max()
+        err = np.linalg.norm(v_gpu[sl].astype(np.float64) - ref.ravel()) / nrm if nrm > 0 else np.abs(v_gpu[sl]).max()
         assert err <= tol, f"Newton-Schulz unit {i} ({un.rows}x{un.cols}): rel err {err:.3e}"
         worst = max(worst, err)
     return worst
