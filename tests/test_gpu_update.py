@@ -188,27 +188,35 @@ def test_adamw_update_flat(hm, dev, gdt):
     v = np.zeros(n, np.float32)
     wt, mt, vt = (torch.from_numpy(x.copy()).to(dev) for x in (w, m, v))
     w64, m64, v64 = w.astype(np.float64), m.astype(np.float64), v.astype(np.float64)
+    # the ABI takes float32 hyperparameters: the oracle gets the same values
+    f = lambda x: float(np.float32(x))  # noqa: E731
+    lr, b1, b2, eps, wd = f(h.lr), f(h.beta1), f(h.beta2), f(h.eps), f(h.weight_decay)
     for step in (1, 2, 3):
         g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
         if gdt == "bf16":
             gb = OM.bf16_rne_bits(g)
             gt = torch.from_numpy(gb.view(np.int16)).to(dev)
-            gx = OM.bf16_bits_to_f32(gb)
+            gx = OM.bf16_bits_to_f32(gb).astype(np.float64)
             code = hm.HM_BF16
         else:
             gt = torch.from_numpy(g).to(dev)
-            gx = g
+            gx = g.astype(np.float64)
             code = hm.HM_F32
         hm.adamw_update_flat(wt.data_ptr(), gt.data_ptr(), code, mt.data_ptr(), vt.data_ptr(), n,
                              adamw_hparams(h, step))
         torch.cuda.synchronize()
-        w_in, m_in = w64, m64
-        w64, m64, v64 = OA.adamw_step(w64, gx, m64, v64, h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, step)
+        w_in, m_in, v_in = w64, m64, v64
+        w64, m64, v64 = OA.adamw_step(w_in, gx, m_in, v_in, lr, b1, b2, eps, wd, step)
         gw, gm, gv = wt.cpu().numpy(), mt.cpu().numpy(), vt.cpu().numpy()
-        # relative error 1e-6 against the magnitudes of the summed terms
-        assert (np.abs(gw - w64) <= 1e-6 * np.maximum(np.abs(w64), np.abs(w_in))).all()
-        assert (np.abs(gm - m64) <= 1e-6 * (np.abs(h.beta1 * m_in) + np.abs((1 - h.beta1) * gx)) + 1e-30).all()
-        assert (np.abs(gv - v64) <= 1e-6 * np.abs(v64) + 1e-30).all()
+        # relative error 1e-6, measured against the magnitude of the terms each
+        # output sums (a forward-error bound: no cancellation is charged)
+        sm = np.abs(b1 * m_in) + np.abs((1 - b1) * gx)
+        sv = np.abs(b2 * v_in) + np.abs((1 - b2) * gx * gx)
+        den = np.sqrt(v64 / (1 - b2 ** step)) + eps
+        sw = np.abs(w_in * (1 - lr * wd)) + lr / (1 - b1 ** step) * sm / den
+        assert (np.abs(gm - m64) <= 1e-6 * sm).all()
+        assert (np.abs(gv - v64) <= 1e-6 * sv).all()
+        assert (np.abs(gw - w64) <= 1e-6 * sw).all()
         # continue from the GPU state so the next step compares like with like
         w64, m64, v64 = gw.astype(np.float64), gm.astype(np.float64), gv.astype(np.float64)
 
