@@ -121,23 +121,21 @@ __global__ void __launch_bounds__(kThreads) f2_kernel(const __grid_constant__ Ra
             while (v >= range_at(ra, ri).prefix + range_at(ra, ri).len) ++ri;
             const Range& r = range_at(ra, ri);
             const int64_t d = v - r.prefix;
-            const float* vp = ((r.flags & 1) ? v_stage : v_root) + r.b + d;
+            const float4* vp = reinterpret_cast<const float4*>(((r.flags & 1) ? v_stage : v_root) + r.b + d);
             float4* wp = reinterpret_cast<float4*>(w + r.a + d);
             const float step = r.step;
+            // all four 16-byte loads are issued before any arithmetic or store
+            const float4 y0 = __ldcs(vp), y1 = __ldcs(vp + 1);
+            float4 x0 = __ldcs(wp), x1 = __ldcs(wp + 1);
+            float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float4 x = __ldcs(wp + h);
-                const float4 y = __ldcs(reinterpret_cast<const float4*>(vp) + h);
-                if (has_decay) {
-                    x.x = __fmul_rn(x.x, decay); x.y = __fmul_rn(x.y, decay);
-                    x.z = __fmul_rn(x.z, decay); x.w = __fmul_rn(x.w, decay);
-                }
-                x.x = __fsub_rn(x.x, __fmul_rn(step, y.x));
-                x.y = __fsub_rn(x.y, __fmul_rn(step, y.y));
-                x.z = __fsub_rn(x.z, __fmul_rn(step, y.z));
-                x.w = __fsub_rn(x.w, __fmul_rn(step, y.w));
-                wp[h] = x;
+            for (int k = 0; k < 8; ++k) {
+                if (has_decay) xv[k] = __fmul_rn(xv[k], decay);
+                xv[k] = __fsub_rn(xv[k], __fmul_rn(step, yv[k]));
             }
+            __stcs(wp, make_float4(xv[0], xv[1], xv[2], xv[3]));
+            __stcs(wp + 1, make_float4(xv[4], xv[5], xv[6], xv[7]));
         }
     }
 }

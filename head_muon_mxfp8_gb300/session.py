@@ -115,6 +115,28 @@ class MuonSession:
                 out[e:e + ln].copy_(root[b:b + ln])
         return out.cpu()
 
+    def fetch_range(self, field: str, a: int, b: int) -> torch.Tensor:
+        """Logical elements [a, b) of a field (on the host); for the scale
+        field a and b count scales."""
+        root = self._root(field)
+        div = 32 if field == "s" else 1
+        out = torch.empty(b - a, dtype=root.dtype, device=self.device)
+        for r in range(self.so):
+            c = self.chunk_of[r]
+            e0, e1 = self.edges[c] // div, self.edges[c + 1] // div
+            lo, hi = max(a, e0), min(b, e1)
+            if lo < hi:
+                base = self.bases[r] // div
+                out[lo - a:hi - a].copy_(root[base + lo - e0:base + hi - e0])
+        return out.cpu()
+
+    def unit_v(self, unit: int) -> torch.Tensor:
+        """The direction v of one unit in logical order (root or staging)."""
+        o, r, c = self.units[unit]
+        if abi.muon_plan_unit(self.plan, unit)["local"]:
+            return self.fetch_range("v", o, o + r * c)
+        return self.staging(unit)[1].cpu()
+
     def canary_intact(self) -> Dict[str, bool]:
         ok = {}
         mask = torch.ones(self.total, dtype=torch.bool, device=self.device)

@@ -1,0 +1,127 @@
+"""Parity at the full workload sizes, in the launch configuration the
+benchmark times (one muon_update_units call over the whole tensor list):
+sampled units through Newton-Schulz, sampled elements through f0 and f2,
+sampled MXFP8 blocks, canaries and the device error word.  The oracle sees
+the exact device inputs (copied back)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads  # noqa: E402
+from oracle import adamw as OA  # noqa: E402
+from oracle import muon as OM  # noqa: E402
+from oracle import mxfp8 as OX  # noqa: E402
+
+from muon_parity import NS_TOL  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(hm):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def _sample_units(cfg, s, hm, rng):
+    """A head (or smallest) unit, a straddling unit and a largest unit."""
+    sizes = [u.numel for u in cfg.units]
+    small = int(np.argmin(sizes))
+    big = int(np.argmax(sizes))
+    strad = [i for i in range(len(cfg.units)) if not hm.muon_plan_unit(s.plan, i)["local"]]
+    pick = {small, big}
+    if strad:
+        pick.add(int(rng.choice(strad)))
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("name", ["lm_layer", "moe_layer", "video_dit"])
+def test_fullsize_update_sampled(hm, dev, name):
+    from head_muon_mxfp8_gb300.session import MuonSession, muon_hparams
+    cfg = workloads.get(name)
+    rng = np.random.default_rng(7)
+    s = MuonSession.from_config(cfg, device=dev)
+    data = workloads.generate_device(cfg, dev, seed=3)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    m0 = torch.empty(cfg.numel, dtype=torch.float32, device=dev).normal_(0.0, 1e-3, generator=gen)
+    s.load("w", data["w"])
+    s.load("g", data["g"])
+    s.load("m", m0)
+    # the samples the oracle will need, taken before the update
+    idx = torch.from_numpy(np.sort(rng.choice(cfg.numel, 1 << 20, replace=False))).to(dev)
+    w0_s, g_s, m0_s = data["w"][idx].cpu().numpy(), data["g"][idx].cpu().numpy(), m0[idx].cpu().numpy()
+    units = _sample_units(cfg, s, hm, rng)
+    w0_units = {i: data["w"][cfg.units[i].offset:cfg.units[i].offset + cfg.units[i].numel].cpu().numpy()
+                for i in units}
+    del data, m0
+    s.run(muon_hparams(cfg.muon))
+    torch.cuda.synchronize()
+    assert hm.hm_device_error() == 0
+    # f0 on sampled elements (bit-exact)
+    m_ref, u_ref = OM.momentum(m0_s, g_s, cfg.muon.momentum)
+    m_all = s.fetch("m")
+    u_all = s.fetch("u")
+    assert np.array_equal(m_all[idx.cpu()].numpy().view(np.uint32), m_ref.view(np.uint32))
+    assert np.array_equal(u_all[idx.cpu()].numpy().view(np.uint16), u_ref)
+    # Newton-Schulz and f2 on whole sampled units
+    h = cfg.muon
+    for i in units:
+        un = cfg.units[i]
+        u_bits = u_all[un.offset:un.offset + un.numel].numpy().view(np.uint16)
+        ref = OM.newton_schulz(OM.bf16_bits_to_f32(u_bits).reshape(un.rows, un.cols), h.ns_steps, h.ns_a, h.ns_b,
+                               h.ns_c, h.eps)
+        v = s.unit_v(i).numpy()
+        err = np.linalg.norm(v.astype(np.float64) - ref.ravel()) / np.linalg.norm(ref)
+        assert err <= NS_TOL, f"unit {i} {un.rows}x{un.cols}: {err:.3e}"
+        w1 = s.fetch_range("w", un.offset, un.offset + un.numel).numpy()
+        want = OM.main_weight_update(w0_units[i], v, h.lr, 1.0)
+        assert np.array_equal(w1.view(np.uint32), want.view(np.uint32))
+    del m_all, u_all
+    # MXFP8 on sampled blocks (bit-exact on the device's updated w)
+    w_all = s.fetch("w").numpy()
+    q_all = s.fetch("q").numpy()
+    s_all = s.fetch("s").numpy()
+    blocks = rng.choice(cfg.numel // 32, 8192, replace=False)
+    for b in blocks[:8192]:
+        codes, sc = OX.quantize_block(w_all[32 * b:32 * b + 32])
+        assert np.array_equal(q_all[32 * b:32 * b + 32], codes) and s_all[b] == sc
+    assert all(s.canary_intact().values())
+    s.close()
+
+
+def test_fullsize_adamw_and_requant_sampled(hm, dev):
+    from head_muon_mxfp8_gb300.session import adamw_hparams
+    cfg = workloads.flat_adamw()
+    n = cfg.numel
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(9)
+    w = torch.empty(n, device=dev).normal_(0, cfg.w_std, generator=gen)
+    g = torch.empty(n, device=dev).normal_(0, cfg.g_std, generator=gen).to(torch.bfloat16)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    rng = np.random.default_rng(1)
+    idx = torch.from_numpy(np.sort(rng.choice(n, 1 << 20, replace=False))).to(dev)
+    w0 = w[idx].cpu().numpy().astype(np.float64)
+    g_s = g[idx].float().cpu().numpy().astype(np.float64)
+    h = cfg.adamw
+    hm.adamw_update_flat(w.data_ptr(), g.data_ptr(), hm.HM_BF16, m.data_ptr(), v.data_ptr(), n, adamw_hparams(h, 1))
+    q = torch.empty(n, dtype=torch.uint8, device=dev)
+    sc = torch.empty(n // 32, dtype=torch.uint8, device=dev)
+    hm.mxfp8_requant_packed(w.data_ptr(), q.data_ptr(), sc.data_ptr(), [(0, 0, 0, 16384, 4096)])
+    torch.cuda.synchronize()
+    f = lambda x: float(np.float32(x))  # noqa: E731
+    lr, b1, b2, eps, wd = f(h.lr), f(h.beta1), f(h.beta2), f(h.eps), f(h.weight_decay)
+    w64, m64, v64 = OA.adamw_step(w0, g_s, 0 * w0, 0 * w0, lr, b1, b2, eps, wd, 1)
+    gw = w[idx].cpu().numpy()
+    sm = np.abs((1 - b1) * g_s)
+    sw = np.abs(w0 * (1 - lr * wd)) + lr / (1 - b1) * sm / (np.sqrt(v64 / (1 - b2)) + eps)
+    assert (np.abs(gw - w64) <= 1e-6 * sw).all()
+    assert (np.abs(m[idx].cpu().numpy() - m64) <= 1e-6 * sm).all()
+    wn = w.cpu().numpy()
+    qn, sn = q.cpu().numpy(), sc.cpu().numpy()
+    for b in rng.choice(n // 32, 8192, replace=False):
+        codes, s1 = OX.quantize_block(wn[32 * b:32 * b + 32])
+        assert np.array_equal(qn[32 * b:32 * b + 32], codes) and sn[b] == s1
