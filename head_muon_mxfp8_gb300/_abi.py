@@ -29,6 +29,9 @@ HM_U8, HM_BF16, HM_F32, HM_E4M3 = 0, 1, 2, 3
 HM_SEG_ALIGN = 1024
 HM_SEG_GAP = 1024
 HM_MX_BLOCK = 32
+HM_NOALLOC_MAX_MIN_DIM = 128
+HM_NOALLOC_MAX_MAX_DIM = 8192
+HM_NOALLOC_SCRATCH_BYTES = 8457216
 
 HM_STAGE_F0 = 1
 HM_STAGE_GATHER = 2
@@ -107,6 +110,7 @@ _SIGS = {
     "muon_plan_destroy": (None, [_P]),
     "adamw_update_flat": (C.c_int, [_P, _P, C.c_int, _P, _P, C.c_int64, C.POINTER(hm_adamw_hparams), _P]),
     "mxfp8_requant_packed": (C.c_int, [_P, _P, _P, C.POINTER(hm_mx_tensor), C.c_int, _P]),
+    "newton_schulz_noalloc": (C.c_int, [_P, C.c_int32, C.c_int32, _P, C.POINTER(hm_muon_hparams), _P]),
 }
 
 _lib = None
@@ -264,3 +268,9 @@ def mxfp8_requant_packed(w: int, q: int, scales: int, tensors, stream: int = 0) 
     arr = (hm_mx_tensor * max(1, len(tensors)))(*[hm_mx_tensor(*t) for t in tensors])
     check("mxfp8_requant_packed", lib().mxfp8_requant_packed(_P(w), _P(q), _P(scales), arr, len(tensors),
                                                              _P(stream)))
+
+
+def newton_schulz_noalloc(u: int, rows: int, cols: int, v: int, hp: hm_muon_hparams, stream: int = 0) -> None:
+    """One unit's Newton-Schulz on the library's built-in scratch: for callers
+    that cannot allocate device memory (see include/hm.h)."""
+    check("newton_schulz_noalloc", lib().newton_schulz_noalloc(_P(u), rows, cols, _P(v), C.byref(hp), _P(stream)))

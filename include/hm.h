@@ -246,6 +246,37 @@ typedef struct {
 hm_status mxfp8_requant_packed(const float* w, uint8_t* q, uint8_t* scales,
                                const hm_mx_tensor* tensors, int n, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Newton-Schulz of one unit without any device allocation.  The paper has no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc -- code that runs while a stream is being captured into a CUDA
+ * graph, code inside a framework whose caching allocator already owns all
+ * device memory, and latency-critical paths that must not take the driver's
+ * allocation lock or risk the implicit synchronisation an allocation brings.
+ *
+ * u: device, rows x cols bf16 bit patterns, row-major, 16-byte aligned; v:
+ * device, rows x cols fp32 output, row-major; both caller-owned.  Computes
+ * what the Newton-Schulz stage of muon_update_units computes for one unit
+ * (same kernels): X0 = u / (||u||_F + eps), transposed when rows > cols,
+ * hp->ns_steps iterations of X = aX + (bA + cA^2)X with A = X X^T, v = X.
+ *
+ * Every intermediate lives in one file-scope __device__ array of
+ * HM_NOALLOC_SCRATCH_BYTES bytes that each GPU loading the library holds
+ * until the process exits.  Limits: min(rows, cols) <= HM_NOALLOC_MAX_MIN_DIM
+ * and max(rows, cols) <= HM_NOALLOC_MAX_MAX_DIM, else HM_ERR_WORKSPACE;
+ * rows*cols a multiple of 8 and the alignments above, else HM_ERR_ALIGN.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls on a device share the array and it keeps the last
+ * call's contents (every call overwrites what it reads), so calls that
+ * overlap on the GPU -- on different streams, or concurrent host threads --
+ * race; serialise them.  Launches on `stream`; allocates nothing. */
+#define HM_NOALLOC_MAX_MIN_DIM 128
+#define HM_NOALLOC_MAX_MAX_DIM 8192
+#define HM_NOALLOC_SCRATCH_BYTES 8457216
+hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int32_t cols, float* v,
+                                const hm_muon_hparams* hp, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
