@@ -334,6 +334,7 @@ double alpha_of(int mode, int rows, int cols) {
 
 struct hm_muon_plan {
     hm_chain chain;
+    std::vector<std::vector<int32_t>> sym_tab;  // per class: triangular tile list
     std::vector<hm_unit_desc> units;
     std::vector<UnitPlan> up;
     std::vector<NsClassDev> classes;
@@ -411,6 +412,20 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
         c.first_unit = static_cast<int32_t>(p->ns_units.size());
         int64_t ne = static_cast<int64_t>(c.m) * c.n;
         c.part_len = static_cast<int32_t>(std::min<int64_t>(kPartLen, round_up(ne, 8)));
+        // A = X X^T and B = bA + cAA are symmetric: only output tiles with an
+        // element on or above the diagonal are computed (the epilogue mirrors
+        // them).  Order: bands of 8 tile-rows, column by column in a band.
+        {
+            const int bn = c.mp >= 256 ? 256 : 128;
+            const int tiles_m = c.mp / 128, tiles_n = (c.mp + bn - 1) / bn;
+            std::vector<int32_t> tab;
+            for (int g0 = 0; g0 < tiles_m; g0 += 8)
+                for (int tn = 0; tn < tiles_n; ++tn)
+                    for (int tm = g0; tm < std::min(tiles_m, g0 + 8); ++tm)
+                        if (tn * bn + bn - 1 >= tm * 128) tab.push_back((tm << 16) | tn);
+            c.sym_tiles = static_cast<int32_t>(tab.size());
+            p->sym_tab.push_back(tab);
+        }
         c.parts = static_cast<int32_t>((ne + c.part_len - 1) / c.part_len);
         for (int i : members[k]) {
             const hm_unit_desc& u = units[i];
@@ -495,6 +510,7 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
         c.b_off = take(ab);
         c.part_off = take(static_cast<size_t>(c.n_units) * c.parts * 4);
         c.inv_off = take(static_cast<size_t>(c.n_units) * 4);
+        c.sym_off = take(static_cast<size_t>(c.sym_tiles) * 4);
     }
     p->ws_bytes = std::max<size_t>(off, kWsAlign);
     *out = p;
@@ -586,6 +602,9 @@ extern "C" hm_status muon_plan_upload(hm_muon_plan* p, void* workspace, size_t w
         put(p->off_gather, p->gather_tab.data(), p->gather_tab.size() * sizeof(Range)) != cudaSuccess ||
         put(p->off_nsu, p->ns_units.data(), p->ns_units.size() * sizeof(NsUnit)) != cudaSuccess)
         return HM_ERR_CUDA;
+    for (size_t k = 0; k < p->classes.size(); ++k)
+        if (put(p->classes[k].sym_off, p->sym_tab[k].data(), p->sym_tab[k].size() * 4) != cudaSuccess)
+            return HM_ERR_CUDA;
     p->maps.assign(p->classes.size(), ClassMaps{});
     for (size_t k = 0; k < p->classes.size(); ++k) {
         const NsClassDev& c = p->classes[k];
@@ -664,6 +683,9 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g1.epi = hm::kEpiGram; g1.alpha = 1.f; g1.beta = 0.f;
                 g1.out = bf(c.a_off); g1.out_us = static_cast<int64_t>(c.mp) * c.mp; g1.ld_out = c.mp;
                 g1.err = hm::device_error_word();
+                g1.tile_tab = reinterpret_cast<const int32_t*>(ws + c.sym_off);
+                g1.tab_len = c.sym_tiles;
+                g1.sym = 1;
                 if (hm::launch_ns_gemm(mp.x_a[cur], mp.x_b[cur], g1, mp.bn1, s) != cudaSuccess) return HM_ERR_CUDA;
 
                 hm::GemmParams g2 = g1;

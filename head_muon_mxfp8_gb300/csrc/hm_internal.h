@@ -65,6 +65,8 @@ struct NsClassDev {
     int32_t parts;       // norm partial sums per unit
     int32_t part_len;    // elements per partial (multiple of 8)
     size_t x_off[2], xt_off[2], a_off, b_off, part_off, inv_off;  // workspace bytes
+    int32_t sym_tiles;   // tiles of the mp x mp output on or above the diagonal
+    size_t sym_off;      // workspace bytes: their (tm << 16 | tn) list, L2-friendly order
 };
 
 // Epilogue kinds of the Newton-Schulz GEMM.
@@ -88,6 +90,9 @@ struct GemmParams {
     float* v_stage;
     int32_t m_real, n_real;
     int32_t* err;
+    const int32_t* tile_tab;  // optional tile list per unit ((tm << 16) | tn); nullptr = full grid
+    int32_t tab_len;
+    int32_t sym;              // symmetric output: write (i, j) and (j, i) for j >= i only
 };
 
 // ---- launchers (return cudaGetLastError() of the launch) -----------------

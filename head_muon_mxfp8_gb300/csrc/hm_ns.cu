@@ -255,6 +255,13 @@ struct GemmCfg {
 };
 
 __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, int& u, int& tm, int& tn) {
+    if (p.tile_tab) {
+        u = t / p.tab_len;
+        const int32_t e = __ldg(p.tile_tab + (t - u * p.tab_len));
+        tm = e >> 16;
+        tn = e & 0xFFFF;
+        return;
+    }
     const int per = p.tiles_m * p.tiles_n;
     u = t / per;
     const int r = t - u * per;
@@ -284,9 +291,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm
     for (int c = 0; c < BN / 32; ++c) {
         const int j0 = tn * BN + c * 32;
         uint32_t r[32];
+        __syncwarp();
         tmem_ld32(taddr + c * 32, r);
         tmem_ld_wait();
         if (j0 >= p.N) continue;  // warp-uniform; N is a multiple of 32
+        const int i0 = i - (threadIdx.x & 31);  // first row of this warp
+        if (p.sym && j0 + 32 <= i0) continue;   // symmetric output: chunk below the diagonal
         float v[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * p.alpha;
@@ -316,6 +326,21 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm
             }
             continue;
         }
+        if (p.sym) {
+            // symmetric output: this warp owns rows i0..i0+31; only elements
+            // with j >= i are written, each to (i, j) and (j, i)
+            uint16_t* ob = p.out + u * p.out_us;
+            if (j0 < i0 + 32) {                            // the diagonal 32 x 32 block
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if (j0 + k >= i) {
+                        const uint16_t b = static_cast<uint16_t>(bf16_bits(v[k]));
+                        ob[static_cast<int64_t>(i) * p.ld_out + j0 + k] = b;
+                        ob[static_cast<int64_t>(j0 + k) * p.ld_out + i] = b;
+                    }
+                continue;
+            }
+        }
         uint4 pk[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -326,12 +351,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm
         uint4* op = reinterpret_cast<uint4*>(p.out + u * p.out_us + static_cast<int64_t>(i) * p.ld_out + j0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) op[q] = pk[q];
-        if (p.epi == kEpiUpdate) {
-            uint16_t* tp = p.out_t + u * p.out_t_us + static_cast<int64_t>(j0) * p.ld_out_t + i;
+        if (p.epi == kEpiUpdate || p.sym) {
+            // transposed copy: X^T for the update, the mirror half for a symmetric output
+            uint16_t* tp = p.epi == kEpiUpdate
+                               ? p.out_t + u * p.out_t_us + static_cast<int64_t>(j0) * p.ld_out_t + i
+                               : p.out + u * p.out_us + static_cast<int64_t>(j0) * p.ld_out + i;
+            const int64_t ldt = p.epi == kEpiUpdate ? p.ld_out_t : p.ld_out;
             const uint32_t* w = reinterpret_cast<const uint32_t*>(pk);
 #pragma unroll
             for (int k = 0; k < 32; ++k)
-                tp[static_cast<int64_t>(k) * p.ld_out_t] = static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
+                tp[static_cast<int64_t>(k) * ldt] = static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
         }
     }
 }
@@ -377,7 +406,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int total = p.units * p.tiles_m * p.tiles_n;
+    const int total = p.units * (p.tile_tab ? p.tab_len : p.tiles_m * p.tiles_n);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -473,7 +502,7 @@ cudaError_t launch_gemm_bn(const CUtensorMap& tma, const CUtensorMap& tmb, const
     p.tiles_m = (p.M + BM - 1) / BM;
     p.tiles_n = (p.N + BN - 1) / BN;
     p.num_kb = (p.K + BK - 1) / BK;
-    const int total = p.units * p.tiles_m * p.tiles_n;
+    const int total = p.units * (p.tile_tab ? p.tab_len : p.tiles_m * p.tiles_n);
     if (total == 0) return cudaSuccess;
     const int grid = total < device_sm_count() ? total : device_sm_count();
     ns_gemm_kernel<BN><<<grid, kGemmThreads, C::SMEM, st>>>(tma, tmb, p);
