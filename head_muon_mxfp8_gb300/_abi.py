@@ -31,7 +31,7 @@ HM_SEG_GAP = 1024
 HM_MX_BLOCK = 32
 HM_NOALLOC_MAX_MIN_DIM = 128
 HM_NOALLOC_MAX_MAX_DIM = 8192
-HM_NOALLOC_SCRATCH_BYTES = 8457216
+HM_NOALLOC_SCRATCH_BYTES = 4262912
 
 HM_STAGE_F0 = 1
 HM_STAGE_GATHER = 2

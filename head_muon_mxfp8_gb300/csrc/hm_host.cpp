@@ -320,7 +320,7 @@ struct UnitPlan {
 };
 
 struct ClassMaps {
-    CUtensorMap x_a[2], x_b[2], a_a, a_b, b_a, xt_b[2];
+    CUtensorMap x_a[2], x_b[2], a_a, a_b, b_a, x_mn[2];
     int bn1 = 128, bn3 = 128;
 };
 
@@ -504,8 +504,6 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
         size_t ab = static_cast<size_t>(c.n_units) * c.mp * c.mp * 2;
         c.x_off[0] = take(xb);
         c.x_off[1] = take(xb);
-        c.xt_off[0] = take(xb);
-        c.xt_off[1] = take(xb);
         c.a_off = take(ab);
         c.b_off = take(ab);
         c.part_off = take(static_cast<size_t>(c.n_units) * c.parts * 4);
@@ -615,7 +613,7 @@ extern "C" hm_status muon_plan_upload(hm_muon_plan* p, void* workspace, size_t w
         for (int b = 0; b < 2; ++b) {
             ok = ok && encode_bf16_3d(&mp.x_a[b], ws + c.x_off[b], c.np, c.mp, c.n_units, 128);
             ok = ok && encode_bf16_3d(&mp.x_b[b], ws + c.x_off[b], c.np, c.mp, c.n_units, mp.bn1);
-            ok = ok && encode_bf16_3d(&mp.xt_b[b], ws + c.xt_off[b], c.mp, c.np, c.n_units, mp.bn3);
+            ok = ok && encode_bf16_3d(&mp.x_mn[b], ws + c.x_off[b], c.np, c.mp, c.n_units, 64);
         }
         ok = ok && encode_bf16_3d(&mp.a_a, ws + c.a_off, c.mp, c.mp, c.n_units, 128);
         ok = ok && encode_bf16_3d(&mp.a_b, ws + c.a_off, c.mp, c.mp, c.n_units, mp.bn1);
@@ -686,14 +684,14 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g1.tile_tab = reinterpret_cast<const int32_t*>(ws + c.sym_off);
                 g1.tab_len = c.sym_tiles;
                 g1.sym = 1;
-                if (hm::launch_ns_gemm(mp.x_a[cur], mp.x_b[cur], g1, mp.bn1, s) != cudaSuccess) return HM_ERR_CUDA;
+                if (hm::launch_ns_gemm(mp.x_a[cur], mp.x_b[cur], g1, mp.bn1, 0, s) != cudaSuccess) return HM_ERR_CUDA;
 
                 hm::GemmParams g2 = g1;
                 g2.K = c.mp;
                 g2.epi = hm::kEpiPoly; g2.alpha = hp->ns_c; g2.beta = hp->ns_b;
                 g2.add = bf(c.a_off); g2.add_us = g1.out_us; g2.ld_add = c.mp;
                 g2.out = bf(c.b_off);
-                if (hm::launch_ns_gemm(mp.a_a, mp.a_b, g2, mp.bn1, s) != cudaSuccess) return HM_ERR_CUDA;
+                if (hm::launch_ns_gemm(mp.a_a, mp.a_b, g2, mp.bn1, 0, s) != cudaSuccess) return HM_ERR_CUDA;
 
                 const bool last = it + 1 == hp->ns_steps;
                 hm::GemmParams g3{};
@@ -701,11 +699,10 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g3.epi = last ? hm::kEpiFinal : hm::kEpiUpdate; g3.alpha = 1.f; g3.beta = hp->ns_a;
                 g3.add = bf(c.x_off[cur]); g3.add_us = static_cast<int64_t>(c.mp) * c.np; g3.ld_add = c.np;
                 g3.out = bf(c.x_off[cur ^ 1]); g3.out_us = g3.add_us; g3.ld_out = c.np;
-                g3.out_t = bf(c.xt_off[cur ^ 1]); g3.out_t_us = g3.add_us; g3.ld_out_t = c.mp;
                 g3.ns_units = units_dev; g3.v_root = b->v; g3.v_stage = v_stage;
                 g3.m_real = c.m; g3.n_real = c.n;
                 g3.err = g1.err;
-                if (hm::launch_ns_gemm(mp.b_a, mp.xt_b[cur], g3, mp.bn3, s) != cudaSuccess) return HM_ERR_CUDA;
+                if (hm::launch_ns_gemm(mp.b_a, mp.x_mn[cur], g3, mp.bn3, 1, s) != cudaSuccess) return HM_ERR_CUDA;
                 cur ^= 1;
             }
         }

@@ -64,7 +64,7 @@ struct NsClassDev {
     int32_t first_unit;  // into the NsUnit table
     int32_t parts;       // norm partial sums per unit
     int32_t part_len;    // elements per partial (multiple of 8)
-    size_t x_off[2], xt_off[2], a_off, b_off, part_off, inv_off;  // workspace bytes
+    size_t x_off[2], a_off, b_off, part_off, inv_off;  // workspace bytes
     int32_t sym_tiles;   // tiles of the mp x mp output on or above the diagonal
     size_t sym_off;      // workspace bytes: their (tm << 16 | tn) list, L2-friendly order
 };
@@ -73,7 +73,7 @@ struct NsClassDev {
 enum GemmEpi : int {
     kEpiGram = 0,    // out = bf16(acc)                         (A = X X^T)
     kEpiPoly = 1,    // out = bf16(alpha*acc + beta*add)        (B = b A + c A A)
-    kEpiUpdate = 2,  // out = out_t^T = bf16(acc + beta*add)    (X = a X + B X)
+    kEpiUpdate = 2,  // out = bf16(acc + beta*add)               (X = a X + B X)
     kEpiFinal = 3,   // v   = fp32(acc + beta*add), per-unit destination
 };
 
@@ -83,7 +83,6 @@ struct GemmParams {
     int32_t epi;
     float alpha, beta;
     uint16_t* out;       int64_t out_us;   int32_t ld_out;   // [units][M][N]
-    uint16_t* out_t;     int64_t out_t_us; int32_t ld_out_t; // [units][N][M]
     const uint16_t* add; int64_t add_us;   int32_t ld_add;   // [units][M][N]
     const NsUnit* ns_units;                                   // final: destinations
     float* v_root;
@@ -113,7 +112,8 @@ cudaError_t launch_ns_norm(const NsClassDev& c, const NsUnit* units_dev, const u
                            const uint16_t* u_stage, char* ws, float eps, cudaStream_t st);
 cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
                               const uint16_t* u_stage, char* ws, cudaStream_t st);
+// b_mn: the B operand is MN-major (its map has 64 x 64 boxes, N innermost)
 cudaError_t launch_ns_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p,
-                           int bn, cudaStream_t st);
+                           int bn, int b_mn, cudaStream_t st);
 
 }  // namespace hm

@@ -5,7 +5,7 @@
 // synchronises), code inside a framework that has already handed all device
 // memory to its own caching allocator, and latency-critical paths that must
 // not take the driver's allocation lock or an implicit device
-// synchronisation.  The caller passes u and v; every intermediate (X, X^T,
+// synchronisation.  The caller passes u and v; every intermediate (X,
 // A, B, the norm partials and the unit descriptor) lives in one file-scope
 // __device__ array of fixed size, which every GPU that loads the library
 // holds until the process exits.
@@ -27,13 +27,11 @@ constexpr size_t kSlot = 1024;
 constexpr size_t kXBytes = static_cast<size_t>(kMaxM) * kMaxN * 2;
 constexpr size_t kABytes = static_cast<size_t>(kMaxM) * kMaxM * 2;
 constexpr size_t kPartsBytes = ((static_cast<size_t>(kMaxM) * kMaxN / kPartLen + 1) * 4 + kSlot - 1) / kSlot * kSlot;
-// layout: unit descriptor | X0 | X1 | XT0 | XT1 | A | B | partials | 1/norm
+// layout: unit descriptor | X0 | X1 | A | B | partials | 1/norm
 constexpr size_t kOffUnit = 0;
 constexpr size_t kOffX0 = kSlot;
 constexpr size_t kOffX1 = kOffX0 + kXBytes;
-constexpr size_t kOffXT0 = kOffX1 + kXBytes;
-constexpr size_t kOffXT1 = kOffXT0 + kXBytes;
-constexpr size_t kOffA = kOffXT1 + kXBytes;
+constexpr size_t kOffA = kOffX1 + kXBytes;
 constexpr size_t kOffB = kOffA + kABytes;
 constexpr size_t kOffParts = kOffB + kABytes;
 constexpr size_t kOffInv = kOffParts + kPartsBytes;
@@ -131,20 +129,18 @@ extern "C" hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int3
     c.parts = static_cast<int32_t>((ne + c.part_len - 1) / c.part_len);
     c.x_off[0] = kOffX0;
     c.x_off[1] = kOffX1;
-    c.xt_off[0] = kOffXT0;
-    c.xt_off[1] = kOffXT1;
     c.a_off = kOffA;
     c.b_off = kOffB;
     c.part_off = kOffParts;
     c.inv_off = kOffInv;
     hm::NsUnit* unit_dev = reinterpret_cast<hm::NsUnit*>(ws + kOffUnit);
 
-    CUtensorMap x_map[2], xt_map[2], a_map, b_map;
+    CUtensorMap x_map[2], x_mn[2], a_map, b_map;
     const int bn3 = c.np >= 256 ? 256 : 128;
     bool ok = true;
     for (int b = 0; b < 2; ++b) {
         ok = ok && map_bf16(&x_map[b], ws + c.x_off[b], c.np, c.mp, 128);
-        ok = ok && map_bf16(&xt_map[b], ws + c.xt_off[b], c.mp, c.np, bn3);
+        ok = ok && map_bf16(&x_mn[b], ws + c.x_off[b], c.np, c.mp, 64);
     }
     ok = ok && map_bf16(&a_map, ws + c.a_off, c.mp, c.mp, 128);
     ok = ok && map_bf16(&b_map, ws + c.b_off, c.mp, c.mp, 128);
@@ -163,14 +159,14 @@ extern "C" hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int3
         g1.epi = hm::kEpiGram; g1.alpha = 1.f; g1.beta = 0.f;
         g1.out = bf(c.a_off); g1.out_us = static_cast<int64_t>(c.mp) * c.mp; g1.ld_out = c.mp;
         g1.err = hm::device_error_word();
-        if (hm::launch_ns_gemm(x_map[cur], x_map[cur], g1, 128, st) != cudaSuccess) return HM_ERR_CUDA;
+        if (hm::launch_ns_gemm(x_map[cur], x_map[cur], g1, 128, 0, st) != cudaSuccess) return HM_ERR_CUDA;
 
         hm::GemmParams g2 = g1;
         g2.K = c.mp;
         g2.epi = hm::kEpiPoly; g2.alpha = hp->ns_c; g2.beta = hp->ns_b;
         g2.add = bf(c.a_off); g2.add_us = g1.out_us; g2.ld_add = c.mp;
         g2.out = bf(c.b_off);
-        if (hm::launch_ns_gemm(a_map, a_map, g2, 128, st) != cudaSuccess) return HM_ERR_CUDA;
+        if (hm::launch_ns_gemm(a_map, a_map, g2, 128, 0, st) != cudaSuccess) return HM_ERR_CUDA;
 
         const bool last = it + 1 == hp->ns_steps;
         hm::GemmParams g3{};
@@ -178,11 +174,10 @@ extern "C" hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int3
         g3.epi = last ? hm::kEpiFinal : hm::kEpiUpdate; g3.alpha = 1.f; g3.beta = hp->ns_a;
         g3.add = bf(c.x_off[cur]); g3.add_us = static_cast<int64_t>(c.mp) * c.np; g3.ld_add = c.np;
         g3.out = bf(c.x_off[cur ^ 1]); g3.out_us = g3.add_us; g3.ld_out = c.np;
-        g3.out_t = bf(c.xt_off[cur ^ 1]); g3.out_t_us = g3.add_us; g3.ld_out_t = c.mp;
         g3.ns_units = unit_dev; g3.v_root = v; g3.v_stage = nullptr;
         g3.m_real = m; g3.n_real = n;
         g3.err = g1.err;
-        if (hm::launch_ns_gemm(b_map, xt_map[cur], g3, bn3, st) != cudaSuccess) return HM_ERR_CUDA;
+        if (hm::launch_ns_gemm(b_map, x_mn[cur], g3, bn3, 1, st) != cudaSuccess) return HM_ERR_CUDA;
         cur ^= 1;
     }
     return HM_OK;

@@ -11,17 +11,18 @@
 // TMEM); the last product is written to v in fp32.
 //
 // Layout in the workspace, per shape class of U units:
-//   X[2], XT[2]  bf16 [U][mp][np] / [U][np][mp]   (ping-pong; XT = X^T)
-//   A, B         bf16 [U][mp][mp]
+//   X[2]   bf16 [U][mp][np]   (ping-pong)
+//   A, B   bf16 [U][mp][mp]
 // with mp = m rounded up to 128 and np = n rounded up to 64; the padding is
-// zero and stays zero.  Keeping X and X^T both row-major lets every GEMM read
-// both operands K-major: A = X X^T contracts X rows with X rows, A A
-// contracts A rows with A rows (A is symmetric), B X contracts B rows with
-// X^T rows.
+// zero and stays zero.  A = X X^T contracts rows of X with rows of X and A A
+// rows of A with rows of A (A is symmetric): both operands K-major.  B X
+// contracts rows of B with columns of X: B is K-major, X is read as an
+// MN-major operand (N contiguous), so X^T is never stored.
 //
 // GEMM kernel: persistent, one CTA per SM, 192 threads:
-//   warp 0      TMA producer: 128x64 and BNx64 bf16 boxes, 128-byte swizzle,
-//               STAGES-deep mbarrier ring;
+//   warp 0      TMA producer: a 128x64 A box and a BNx64 K-major B box (or
+//               BN/64 boxes of 64 N x 64 K for an MN-major B), 128-byte
+//               swizzle, STAGES-deep mbarrier ring;
 //   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=16)
 //               from one lane into a double-buffered fp32 accumulator;
 //   warps 2-5   epilogue: tcgen05.ld 32x32b rows out of TMEM, fused
@@ -86,14 +87,14 @@ __global__ void ns_norm_final_kernel(const float* __restrict__ partials, int par
 }
 
 // ---------------------------------------------------------------------------
-// X0 and X0^T from u: 64x64 tiles of X coordinates through shared memory,
-// coalesced reads of u in either orientation, coalesced writes of X and X^T.
+// X0 from u: 64x64 tiles of X coordinates through shared memory, coalesced
+// reads of u in either orientation, coalesced writes of X.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) ns_prepare_kernel(const NsUnit* __restrict__ units,
                                                           const uint16_t* __restrict__ u_root,
                                                           const uint16_t* __restrict__ u_stage,
                                                           const float* __restrict__ inv, uint16_t* __restrict__ X,
-                                                          uint16_t* __restrict__ XT, int m, int n, int mp, int np) {
+                                                          int m, int n, int np) {
     __shared__ uint16_t T[64][66];
     const int unit = blockIdx.z;
     const NsUnit nu = units[unit];
@@ -114,15 +115,10 @@ __global__ void __launch_bounds__(256) ns_prepare_kernel(const NsUnit* __restric
         T[ii][jj] = val;
     }
     __syncthreads();
-    uint16_t* xo = X + static_cast<int64_t>(unit) * mp * np;
-    uint16_t* to = XT + static_cast<int64_t>(unit) * mp * np;
+    uint16_t* xo = X + static_cast<int64_t>(unit) * gridDim.y * 64 * np;
     for (int idx = threadIdx.x; idx < 64 * 64; idx += 256) {
         const int ii = idx >> 6, jj = idx & 63;
         xo[static_cast<int64_t>(i0 + ii) * np + j0 + jj] = T[ii][jj];
-    }
-    for (int idx = threadIdx.x; idx < 64 * 64; idx += 256) {
-        const int jj = idx >> 6, ii = idx & 63;
-        to[static_cast<int64_t>(j0 + jj) * mp + i0 + ii] = T[ii][jj];
     }
 }
 
@@ -240,18 +236,31 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
-template <int BN>
+// The same for an MN-major operand (N contiguous) loaded as BN/64 TMA boxes of
+// 64 N x 64 K, each box 64 rows (one per K) of 128 B: 8-K-row atoms of 1024 B
+// (stride-dimension byte offset 1024), consecutive 64-element N chunks 8 KiB
+// apart (leading-dimension byte offset 8192).  Advancing K by 16 rows adds
+// 2048 bytes to the start address.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(8192 >> 4) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+template <int BN, bool B_MN>
 struct GemmCfg {
     static constexpr int STAGES = BN == 256 ? 4 : 6;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
-    // kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major,
-    // N >> 3 at bit 17, M >> 4 at bit 24.
-    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+    // kind::f16 instruction descriptor: D fp32, A and B bf16, A K-major, B
+    // K-major or (bit 16) MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
+    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (B_MN ? (1u << 16) : 0u) |
                                       (static_cast<uint32_t>(BN >> 3) << 17) |
                                       (static_cast<uint32_t>(BM >> 4) << 24);
+    // descriptor start-address step (16-byte units) per K = 16 MMA
+    static constexpr uint64_t B_KSTEP = B_MN ? (2048 >> 4) : (32 >> 4);
 };
 
 __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, int& u, int& tm, int& tn) {
@@ -351,25 +360,22 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm
         uint4* op = reinterpret_cast<uint4*>(p.out + u * p.out_us + static_cast<int64_t>(i) * p.ld_out + j0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) op[q] = pk[q];
-        if (p.epi == kEpiUpdate || p.sym) {
-            // transposed copy: X^T for the update, the mirror half for a symmetric output
-            uint16_t* tp = p.epi == kEpiUpdate
-                               ? p.out_t + u * p.out_t_us + static_cast<int64_t>(j0) * p.ld_out_t + i
-                               : p.out + u * p.out_us + static_cast<int64_t>(j0) * p.ld_out + i;
-            const int64_t ldt = p.epi == kEpiUpdate ? p.ld_out_t : p.ld_out;
+        if (p.sym) {
+            // the mirror half of a symmetric output: (j, i) for every (i, j) above
+            uint16_t* tp = p.out + u * p.out_us + static_cast<int64_t>(j0) * p.ld_out + i;
             const uint32_t* w = reinterpret_cast<const uint32_t*>(pk);
 #pragma unroll
             for (int k = 0; k < 32; ++k)
-                tp[static_cast<int64_t>(k) * ldt] = static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
+                tp[static_cast<int64_t>(k) * p.ld_out] = static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
         }
     }
 }
 
-template <int BN>
+template <int BN, bool B_MN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     ns_gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                    const __grid_constant__ GemmParams p) {
-    using C = GemmCfg<BN>;
+    using C = GemmCfg<BN, B_MN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sa = smem;
@@ -421,7 +427,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t fb = smem_u32(&full[s]);
                     mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
                     tma_load_3d(smem_u32(sa + s * C::A_BYTES), &tma, fb, kb * BK, tm * BM, u);
-                    tma_load_3d(smem_u32(sb + s * C::B_BYTES), &tmb, fb, kb * BK, tn * BN, u);
+                    if (B_MN) {
+#pragma unroll
+                        for (int c = 0; c < BN / 64; ++c)
+                            tma_load_3d(smem_u32(sb + s * C::B_BYTES + c * 8192), &tmb, fb, tn * BN + c * 64, kb * BK,
+                                        u);
+                    } else {
+                        tma_load_3d(smem_u32(sb + s * C::B_BYTES), &tmb, fb, kb * BK, tn * BN, u);
+                    }
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                     if (++s == C::STAGES) { s = 0; ph ^= 1u; }
@@ -444,10 +457,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (!mbar_wait(smem_u32(&full[s]), ph, p.err, bail)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ad = desc_sw128(smem_u32(sa + s * C::A_BYTES));
-                    const uint64_t bd = desc_sw128(smem_u32(sb + s * C::B_BYTES));
+                    const uint32_t bs = smem_u32(sb + s * C::B_BYTES);
+                    const uint64_t bd = B_MN ? desc_mn_sw128(bs) : desc_sw128(bs);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16(d, ad + 2 * kk, bd + 2 * kk, C::IDESC, (kb | kk) != 0);
+                        umma_bf16(d, ad + 2 * kk, bd + C::B_KSTEP * kk, C::IDESC, (kb | kk) != 0);
                     umma_commit(smem_u32(&empty[s]));
                     if (++s == C::STAGES) { s = 0; ph ^= 1u; }
                 }
@@ -487,14 +501,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <int BN>
+template <int BN, bool B_MN>
 cudaError_t launch_gemm_bn(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p0, cudaStream_t st) {
-    using C = GemmCfg<BN>;
+    using C = GemmCfg<BN, B_MN>;
     static bool configured[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<BN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
@@ -505,7 +519,7 @@ cudaError_t launch_gemm_bn(const CUtensorMap& tma, const CUtensorMap& tmb, const
     const int total = p.units * (p.tile_tab ? p.tab_len : p.tiles_m * p.tiles_n);
     if (total == 0) return cudaSuccess;
     const int grid = total < device_sm_count() ? total : device_sm_count();
-    ns_gemm_kernel<BN><<<grid, kGemmThreads, C::SMEM, st>>>(tma, tmb, p);
+    ns_gemm_kernel<BN, B_MN><<<grid, kGemmThreads, C::SMEM, st>>>(tma, tmb, p);
     return cudaGetLastError();
 }
 
@@ -527,14 +541,14 @@ cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, cons
                               const uint16_t* u_stage, char* ws, cudaStream_t st) {
     dim3 g(c.np / 64, c.mp / 64, c.n_units);
     ns_prepare_kernel<<<g, 256, 0, st>>>(units_dev, u_root, u_stage, reinterpret_cast<const float*>(ws + c.inv_off),
-                                         reinterpret_cast<uint16_t*>(ws + c.x_off[0]),
-                                         reinterpret_cast<uint16_t*>(ws + c.xt_off[0]), c.m, c.n, c.mp, c.np);
+                                         reinterpret_cast<uint16_t*>(ws + c.x_off[0]), c.m, c.n, c.np);
     return cudaGetLastError();
 }
 
-cudaError_t launch_ns_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p, int bn,
+cudaError_t launch_ns_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p, int bn, int b_mn,
                            cudaStream_t st) {
-    return bn == 256 ? launch_gemm_bn<256>(tma, tmb, p, st) : launch_gemm_bn<128>(tma, tmb, p, st);
+    if (b_mn) return bn == 256 ? launch_gemm_bn<256, true>(tma, tmb, p, st) : launch_gemm_bn<128, true>(tma, tmb, p, st);
+    return bn == 256 ? launch_gemm_bn<256, false>(tma, tmb, p, st) : launch_gemm_bn<128, false>(tma, tmb, p, st);
 }
 
 }  // namespace hm
