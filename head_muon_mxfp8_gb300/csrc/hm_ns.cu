@@ -87,38 +87,63 @@ __global__ void ns_norm_final_kernel(const float* __restrict__ partials, int par
 }
 
 // ---------------------------------------------------------------------------
-// X0 from u: 64x64 tiles of X coordinates through shared memory, coalesced
-// reads of u in either orientation, coalesced writes of X.
+// X0 from u: 64x64 tiles of X coordinates through shared memory.  Both the
+// read of u (in either orientation) and the write of X move 16-byte vectors
+// of 8 bf16 when the row length allows it (n, resp. m, a multiple of 8).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint16_t scale_bf16(uint16_t raw, float s) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(static_cast<uint32_t>(raw) << 16) * s));
+}
+
 __global__ void __launch_bounds__(256) ns_prepare_kernel(const NsUnit* __restrict__ units,
                                                           const uint16_t* __restrict__ u_root,
                                                           const uint16_t* __restrict__ u_stage,
                                                           const float* __restrict__ inv, uint16_t* __restrict__ X,
                                                           int m, int n, int np) {
-    __shared__ uint16_t T[64][66];
+    __shared__ __align__(16) uint16_t T[64][72];  // X orientation; 144-byte rows keep 16-byte alignment
     const int unit = blockIdx.z;
     const NsUnit nu = units[unit];
     const uint16_t* src = ((nu.flags & kNsUStaged) ? u_stage : u_root) + nu.u_off;
     const bool tr = nu.flags & kNsTransposed;
     const float s = inv[unit];
     const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
-    for (int idx = threadIdx.x; idx < 64 * 64; idx += 256) {
-        int ii, jj;
-        if (!tr) { ii = idx >> 6; jj = idx & 63; }
-        else { jj = idx >> 6; ii = idx & 63; }
-        const int i = i0 + ii, j = j0 + jj;
-        uint16_t val = 0;
-        if (i < m && j < n) {
-            const uint16_t raw = tr ? src[static_cast<int64_t>(j) * m + i] : src[static_cast<int64_t>(i) * n + j];
-            val = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(static_cast<uint32_t>(raw) << 16) * s));
+    // u row r has length ld and 64 consecutive X entries of one tile row map to
+    // 64 consecutive u entries of one u row (non-transposed) or of one u column
+    const int ld = tr ? m : n;
+    const bool vec_ok = (ld & 7) == 0;
+    for (int v = threadIdx.x; v < 512; v += 256) {
+        const int a = v >> 3, b0 = (v & 7) * 8;  // u-tile row a, 8 entries from b0
+        // non-transposed: u row i0+a, cols j0+b0..; transposed: u row j0+a, cols i0+b0..
+        const int ur = (tr ? j0 : i0) + a, uc = (tr ? i0 : j0) + b0;
+        const int rlim = tr ? n : m, clim = tr ? m : n;
+        uint16_t e[8];
+        if (ur < rlim && vec_ok && uc + 8 <= clim) {
+            const uint4 x = __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(ur) * ld + uc));
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                e[2 * k] = scale_bf16(static_cast<uint16_t>(w[k] & 0xFFFFu), s);
+                e[2 * k + 1] = scale_bf16(static_cast<uint16_t>(w[k] >> 16), s);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                e[k] = (ur < rlim && uc + k < clim) ? scale_bf16(src[static_cast<int64_t>(ur) * ld + uc + k], s) : 0;
         }
-        T[ii][jj] = val;
+        if (!tr) {
+            *reinterpret_cast<uint4*>(&T[a][b0]) = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16),
+                                                              e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) T[b0 + k][a] = e[k];
+        }
     }
     __syncthreads();
     uint16_t* xo = X + static_cast<int64_t>(unit) * gridDim.y * 64 * np;
-    for (int idx = threadIdx.x; idx < 64 * 64; idx += 256) {
-        const int ii = idx >> 6, jj = idx & 63;
-        xo[static_cast<int64_t>(i0 + ii) * np + j0 + jj] = T[ii][jj];
+    for (int v = threadIdx.x; v < 512; v += 256) {
+        const int ii = v >> 3, jj = (v & 7) * 8;
+        *reinterpret_cast<uint4*>(xo + static_cast<int64_t>(i0 + ii) * np + j0 + jj) =
+            *reinterpret_cast<const uint4*>(&T[ii][jj]);
     }
 }
 
