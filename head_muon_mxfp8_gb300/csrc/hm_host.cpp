@@ -701,6 +701,7 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g3.out = bf(c.x_off[cur ^ 1]); g3.out_us = g3.add_us; g3.ld_out = c.np;
                 g3.ns_units = units_dev; g3.v_root = b->v; g3.v_stage = v_stage;
                 g3.m_real = c.m; g3.n_real = c.n;
+                g3.group_m = c.mp / 128;  // column bands: each X panel is fetched once per unit
                 g3.err = g1.err;
                 if (hm::launch_ns_gemm(mp.b_a, mp.x_mn[cur], g3, mp.bn3, 1, s) != cudaSuccess) return HM_ERR_CUDA;
                 cur ^= 1;

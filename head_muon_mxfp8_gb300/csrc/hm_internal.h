@@ -92,6 +92,7 @@ struct GemmParams {
     const int32_t* tile_tab;  // optional tile list per unit ((tm << 16) | tn); nullptr = full grid
     int32_t tab_len;
     int32_t sym;              // symmetric output: write (i, j) and (j, i) for j >= i only
+    int32_t group_m;          // tile-rows per raster band of the full grid (0 = 8)
 };
 
 // ---- launchers (return cudaGetLastError() of the launch) -----------------

@@ -278,7 +278,8 @@ struct GemmCfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
+    static constexpr int EPI_BYTES = 4 * 32 * 33 * 4;  // per epilogue warp: a 32 x 32 fp32 transpose tile
+    static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + EPI_BYTES + 1024 + 256;
     // kind::f16 instruction descriptor: D fp32, A and B bf16, A K-major, B
     // K-major or (bit 16) MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
     static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (B_MN ? (1u << 16) : 0u) |
@@ -299,10 +300,11 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, int& u, 
     const int per = p.tiles_m * p.tiles_n;
     u = t / per;
     const int r = t - u * per;
-    const int group = 8 * p.tiles_n;
+    const int band = p.group_m > 0 ? p.group_m : 8;
+    const int group = band * p.tiles_n;
     const int g = r / group;
-    const int first = g * 8;
-    const int gm = min(p.tiles_m - first, 8);
+    const int first = g * band;
+    const int gm = min(p.tiles_m - first, band);
     const int rr = r - g * group;
     tm = first + rr % gm;
     tn = rr / gm;
@@ -319,7 +321,8 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& x, float* f) {
 __device__ __forceinline__ uint32_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
 template <int BN>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm, int tn, int row, uint32_t taddr) {
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm, int tn, int row, uint32_t taddr,
+                                              float* stage) {
     const int i = tm * BM + row;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -346,17 +349,28 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm
         }
         if (p.epi == kEpiFinal) {
             const NsUnit nu = p.ns_units[u];
-            if (i < p.m_real) {
+            if (i < p.m_real && (nu.flags & kNsTransposed)) {
                 float* dst = ((nu.flags & kNsVStaged) ? p.v_stage : p.v_root) + nu.v_off;
-                if (nu.flags & kNsTransposed) {
+                {
 #pragma unroll
                     for (int k = 0; k < 32; ++k)
                         if (j0 + k < p.n_real) dst[static_cast<int64_t>(j0 + k) * p.m_real + i] = v[k];
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        if (j0 + k < p.n_real) dst[static_cast<int64_t>(i) * p.n_real + j0 + k] = v[k];
                 }
+            }
+            if (!(nu.flags & kNsTransposed)) {
+                // row-major v: transpose the warp's 32 x 32 block through shared
+                // memory so that each store instruction writes 128 contiguous bytes
+                const int lane = threadIdx.x & 31;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) stage[lane * 33 + k] = v[k];
+                __syncwarp();
+                float* dst = ((nu.flags & kNsVStaged) ? p.v_stage : p.v_root) + nu.v_off;
+                if (j0 + lane < p.n_real) {
+#pragma unroll 4
+                    for (int r2 = 0; r2 < 32; ++r2)
+                        if (i0 + r2 < p.m_real) dst[static_cast<int64_t>(i0 + r2) * p.n_real + j0 + lane] = stage[r2 * 33 + lane];
+                }
+                __syncwarp();
             }
             continue;
         }
@@ -405,7 +419,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sa = smem;
     uint8_t* sb = sa + C::STAGES * C::A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sb + C::STAGES * C::B_BYTES);
+    float* epi_stage = reinterpret_cast<float*>(sb + C::STAGES * C::B_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sb + C::STAGES * C::B_BYTES + C::EPI_BYTES);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
     uint64_t* tfull = bars + 2 * C::STAGES;
@@ -511,8 +526,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            epilogue_tile<BN>(p, u, tm, tn, row, tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                                                      static_cast<uint32_t>(acc * BN));
+            epilogue_tile<BN>(p, u, tm, tn, row,
+                              tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN),
+                              epi_stage + q * 32 * 33);
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[acc]));
             acc ^= 1;
