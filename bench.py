@@ -70,6 +70,21 @@ def straddling_elems(cfg, plan_info) -> int:
     return int(plan_info.staging_elems)
 
 
+# DRAM bytes (read + write) of one Newton-Schulz stage of the Video-DiT x8
+# workload, from profiles/video_dit_launch_list_dram.md, valid for the kernel
+# source it was measured on (sha256 prefix of hm_ns.cu).
+NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 169.835e9, "hm_ns_sha256": "8b3ddd80f8956d48"}
+
+
+def ns_stage_traffic(cfg):
+    import hashlib
+    src = os.path.join(ROOT, "head_muon_mxfp8_gb300", "csrc", "hm_ns.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if cfg.name != NS_STAGE_TRAFFIC["workload"] or sha != NS_STAGE_TRAFFIC["hm_ns_sha256"]:
+        return None
+    return NS_STAGE_TRAFFIC["bytes"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -367,7 +382,8 @@ def run_ours(args, cfg):
         kern["adamw_flat_64M"] = adamw
         adamw["frac"] = adamw["gbs"] / peaks["hbm_gbs"]
     roofline = {"bound": "tensor", "achieved": ns_tflops, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                "frac": ns_tflops / peaks["bf16_sustained"], "traffic": None,
+                "frac": ns_tflops / peaks["bf16_sustained"], "traffic": ns_stage_traffic(cfg),
+                "traffic_unit": "DRAM bytes per Newton-Schulz stage (one update), ncu",
                 "kernel": "Newton-Schulz stage (ns_gemm_kernel, 15 launches per shape class, plus norm/prepare)",
                 "peak_kind": f"bf16 dense sustained ({peaks['source']})",
                 "frac_of_burst": ns_tflops / peaks["bf16"],
