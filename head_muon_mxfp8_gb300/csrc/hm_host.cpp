@@ -13,6 +13,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -666,6 +667,12 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
         if (hm::launch_copy_bf16(ra, b->u, u_stage, s) != cudaSuccess) return HM_ERR_CUDA;
     }
     if (stages & HM_STAGE_NS) {
+        // Failure-detection test hook: with HM_INJECT_NS_WAIT_TIMEOUT=1 in the
+        // environment, the first GEMM of this call never marks an accumulator
+        // ready, so its epilogue waits run out (bounded) and the kernel records
+        // HM_ERR_TIMEOUT in the device error word.
+        const char* inj = std::getenv("HM_INJECT_NS_WAIT_TIMEOUT");
+        bool inject = inj && inj[0] == '1';
         for (size_t k = 0; k < p->classes.size(); ++k) {
             const NsClassDev& c = p->classes[k];
             const ClassMaps& mp = p->maps[k];
@@ -684,7 +691,10 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g1.tile_tab = reinterpret_cast<const int32_t*>(ws + c.sym_off);
                 g1.tab_len = c.sym_tiles;
                 g1.sym = 1;
+                g1.inject_no_ready = inject ? 1 : 0;
+                inject = false;
                 if (hm::launch_ns_gemm(mp.x_a[cur], mp.x_b[cur], g1, mp.bn1, 0, s) != cudaSuccess) return HM_ERR_CUDA;
+                g1.inject_no_ready = 0;
 
                 hm::GemmParams g2 = g1;
                 g2.K = c.mp;

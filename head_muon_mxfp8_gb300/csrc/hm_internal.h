@@ -93,6 +93,7 @@ struct GemmParams {
     int32_t tab_len;
     int32_t sym;              // symmetric output: write (i, j) and (j, i) for j >= i only
     int32_t group_m;          // tile-rows per raster band of the full grid (0 = 8)
+    int32_t inject_no_ready;  // failure test: never signal an accumulator as ready
 };
 
 // ---- launchers (return cudaGetLastError() of the launch) -----------------

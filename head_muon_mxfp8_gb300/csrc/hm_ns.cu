@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (++s == C::STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                umma_commit(smem_u32(&tfull[acc]));
+                if (!p.inject_no_ready) umma_commit(smem_u32(&tfull[acc]));
                 acc ^= 1;
                 if (!acc) aph ^= 1u;
             }

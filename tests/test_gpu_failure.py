@@ -1,0 +1,54 @@
+"""Failure detection on the GPU without a fault: a Newton-Schulz GEMM whose
+accumulator is never marked ready (test hook HM_INJECT_NS_WAIT_TIMEOUT) must
+give up on its bounded waits, record HM_ERR_TIMEOUT in the device error
+word, free its resources and return; the context stays usable and the next
+update is correct."""
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads  # noqa: E402
+
+from muon_parity import check_f0, check_ns  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(hm):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def test_injected_wait_timeout_is_reported_and_recovered(hm, dev):
+    from head_muon_mxfp8_gb300.session import MuonSession, muon_hparams
+    cfg = workloads.get("tiny")
+    data = workloads.generate(cfg, seed=41)
+    s = MuonSession.from_config(cfg, device=dev)
+    s.load("w", data["w"])
+    s.load("g", data["g"])
+    s.load("m", np.zeros_like(data["w"]))
+    hp = muon_hparams(cfg.muon)
+    assert hm.hm_device_error() == 0
+    os.environ["HM_INJECT_NS_WAIT_TIMEOUT"] = "1"
+    try:
+        s.run(hp, hm.HM_STAGE_F0 | hm.HM_STAGE_GATHER | hm.HM_STAGE_NS)
+        torch.cuda.synchronize()                  # returns: the waits are bounded
+    finally:
+        del os.environ["HM_INJECT_NS_WAIT_TIMEOUT"]
+    assert hm.hm_device_error() == hm.HM_ERR_TIMEOUT
+    assert hm.hm_device_error() == 0              # read-and-clear
+    # the context is intact: a clean update gives the right answer
+    s.load("m", np.zeros_like(data["w"]))
+    s.run(hp, hm.HM_STAGE_F0 | hm.HM_STAGE_GATHER | hm.HM_STAGE_NS)
+    torch.cuda.synchronize()
+    assert hm.hm_device_error() == 0
+    m = s.fetch("m").numpy()
+    u = s.fetch("u").numpy().view(np.uint16)
+    check_f0(np.zeros_like(data["w"]), data["g"], m, u, cfg.muon.momentum)
+    check_ns(cfg, u, s.fetch("v").numpy(), cfg.muon)
+    s.close()
