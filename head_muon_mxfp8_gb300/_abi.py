@@ -39,6 +39,8 @@ HM_STAGE_NS = 4
 HM_STAGE_F2 = 8
 HM_STAGE_REQUANT = 16
 HM_STAGE_ALL = 31
+HM_STAGE_FUSED = 32
+HM_STAGE_ALL_FUSED = 63
 
 
 class hm_fragment(C.Structure):

@@ -14,6 +14,7 @@
 // moves 16-byte vectors.  Range lengths are multiples of 32 elements, so a
 // vector never crosses a range and a 1x32 MX block never crosses a segment.
 #include "hm_internal.h"
+#include "hm_mx_device.cuh"
 
 #include <cuda_bf16.h>
 
@@ -58,7 +59,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) f0_kernel(const __grid_constant__ RangeArgs ra, float* __restrict__ m,
                                                        const float* __restrict__ g, uint16_t* __restrict__ u,
-                                                       float mu, int nesterov) {
+                                                       uint16_t* __restrict__ u_stage, float mu, int nesterov) {
     for (int64_t t0 = blockIdx.x * kTile; t0 < ra.total; t0 += static_cast<int64_t>(gridDim.x) * kTile) {
         int ri = find_range(ra, t0);
         const int64_t t1 = min(t0 + kTile, ra.total);
@@ -83,6 +84,8 @@ __global__ void __launch_bounds__(kThreads) f0_kernel(const __grid_constant__ Ra
             uint4 pk = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]),
                                   pack_bf16x2(src[4], src[5]), pack_bf16x2(src[6], src[7]));
             *reinterpret_cast<uint4*>(u + e) = pk;
+            // fused gather: a fragment of a straddling unit also lands in its staging
+            if (r.flags & 2) *reinterpret_cast<uint4*>(u_stage + r.b + (v - r.prefix)) = pk;
         }
     }
 }
@@ -148,27 +151,6 @@ __global__ void __launch_bounds__(kThreads) f2_kernel(const __grid_constant__ Ra
 // whenever y is in E4M3 range) are rounded to E4M3 by the hardware's
 // round-to-nearest-even, saturate-to-finite conversion.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int mx_scale_exponent(float amax) {
-    const uint32_t bits = __float_as_uint(amax);
-    const int ex = static_cast<int>(bits >> 23);
-    int fl;
-    if (ex == 0) {
-        const uint32_t mant = bits & 0x7FFFFFu;
-        if (mant == 0) return -127;
-        fl = (31 - __clz(static_cast<int>(mant))) - 149;
-    } else {
-        fl = ex - 127;
-    }
-    const int e = fl - 8;
-    return e < -127 ? -127 : (e > 127 ? 127 : e);
-}
-
-__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
 __global__ void __launch_bounds__(kThreads) requant_kernel(const __grid_constant__ RangeArgs ra,
                                                            const float* __restrict__ w, uint8_t* __restrict__ q,
                                                            uint8_t* __restrict__ s) {
@@ -198,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const __grid_constant
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             if (live) {
                 const int e = mx_scale_exponent(amax);
-                const float sc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, normal
+                const float sc = mx_inv_scale(e);  // 2^-e, a normal fp32
                 const uint32_t c01 = cvt_e4m3x2(x[0] * sc, x[1] * sc);
                 const uint32_t c23 = cvt_e4m3x2(x[2] * sc, x[3] * sc);
                 const uint32_t c45 = cvt_e4m3x2(x[4] * sc, x[5] * sc);
@@ -206,6 +188,64 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const __grid_constant
                 const int64_t d = v - r->prefix;
                 uint2 pk = make_uint2(c01 | (c23 << 16), c45 | (c67 << 16));
                 __stcs(reinterpret_cast<uint2*>(q + r->b + d), pk);
+                if ((lane & 3) == 0) s[(r->c + d) >> 5] = static_cast<uint8_t>(e + 127);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// f2 and G in one pass (fused update, fragments of units whose v went through
+// memory): w <- w*decay - step*v, then the MX block of the new w is quantized.
+// Same lane layout as requant_kernel: four lanes own one 1x32 block.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) f2_requant_kernel(const __grid_constant__ RangeArgs ra,
+                                                              float* __restrict__ w, const float* __restrict__ v_root,
+                                                              const float* __restrict__ v_stage,
+                                                              uint8_t* __restrict__ q, uint8_t* __restrict__ s,
+                                                              float decay, int has_decay) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    for (int64_t t0 = blockIdx.x * kTile; t0 < ra.total; t0 += static_cast<int64_t>(gridDim.x) * kTile) {
+        int ri = find_range(ra, t0);
+        const int64_t t1 = min(t0 + kTile, ra.total);
+        for (int64_t wb = t0 + warp * 256; wb < t1; wb += kThreads * 8) {
+            const int64_t v = wb + lane * 8;
+            const bool live = v < t1;
+            float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const Range* r = nullptr;
+            int64_t d = 0;
+            if (live) {
+                while (v >= range_at(ra, ri).prefix + range_at(ra, ri).len) ++ri;
+                r = &range_at(ra, ri);
+                d = v - r->prefix;
+                const float4* wp = reinterpret_cast<const float4*>(w + r->a + d);
+                const float4* vp = reinterpret_cast<const float4*>(((r->flags & 1) ? v_stage : v_root) + r->b + d);
+                const float4 w0 = __ldcs(wp), w1 = __ldcs(wp + 1), y0 = __ldcs(vp), y1 = __ldcs(vp + 1);
+                const float xv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float a = has_decay ? __fmul_rn(xv[k], decay) : xv[k];
+                    x[k] = __fsub_rn(a, __fmul_rn(r->step, yv[k]));
+                }
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            if (live) {
+                float4* wp = reinterpret_cast<float4*>(w + r->a + d);
+                __stcs(wp, make_float4(x[0], x[1], x[2], x[3]));
+                __stcs(wp + 1, make_float4(x[4], x[5], x[6], x[7]));
+                const int e = mx_scale_exponent(amax);
+                const float sc = mx_inv_scale(e);
+                const uint32_t c01 = cvt_e4m3x2(x[0] * sc, x[1] * sc);
+                const uint32_t c23 = cvt_e4m3x2(x[2] * sc, x[3] * sc);
+                const uint32_t c45 = cvt_e4m3x2(x[4] * sc, x[5] * sc);
+                const uint32_t c67 = cvt_e4m3x2(x[6] * sc, x[7] * sc);
+                __stcs(reinterpret_cast<uint2*>(q + r->a + d), make_uint2(c01 | (c23 << 16), c45 | (c67 << 16)));
                 if ((lane & 3) == 0) s[(r->c + d) >> 5] = static_cast<uint8_t>(e + 127);
             }
         }
@@ -292,10 +332,10 @@ int32_t* device_error_word() {
     return static_cast<int32_t*>(cached[dev]);
 }
 
-cudaError_t launch_f0(const RangeArgs& ra, float* m, const float* g, uint16_t* u, float mu, int nesterov,
-                      cudaStream_t st) {
+cudaError_t launch_f0(const RangeArgs& ra, float* m, const float* g, uint16_t* u, uint16_t* u_stage, float mu,
+                      int nesterov, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
-    f0_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, m, g, u, mu, nesterov);
+    f0_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, m, g, u, u_stage, mu, nesterov);
     return cudaGetLastError();
 }
 
@@ -315,6 +355,13 @@ cudaError_t launch_f2(const RangeArgs& ra, float* w, const float* v_root, const 
 cudaError_t launch_requant(const RangeArgs& ra, const float* w, uint8_t* q, uint8_t* s, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
     requant_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, w, q, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_f2_requant(const RangeArgs& ra, float* w, const float* v_root, const float* v_stage, uint8_t* q,
+                              uint8_t* s, float decay, int has_decay, cudaStream_t st) {
+    if (ra.total == 0) return cudaSuccess;
+    f2_requant_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, w, v_root, v_stage, q, s, decay, has_decay);
     return cudaGetLastError();
 }
 

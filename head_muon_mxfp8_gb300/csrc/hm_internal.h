@@ -24,7 +24,8 @@ struct Range {
     int64_t len;
     int64_t prefix;
     float   step;   // f2: fp32(lr * alpha) of the unit the range belongs to
-    int32_t flags;  // f2: bit 0 = v read from the workspace staging
+    int32_t flags;  // f2: bit 0 = v read from the workspace staging;
+                    // f0: bit 1 = also write u to the staging at b + d
 };
 static_assert(sizeof(Range) == 48, "Range layout");
 
@@ -46,13 +47,15 @@ struct NsUnit {
     int64_t v_off;   // element offset of v in the v root or the v staging
     int32_t rows;    // unit as stored: rows x cols, row-major
     int32_t cols;
-    int32_t flags;   // kNsU* bits
-    int32_t pad;
+    int32_t flags;   // kNs* bits
+    float step;      // fp32(lr * alpha) of the unit (fused f2)
 };
 static_assert(sizeof(NsUnit) == 32, "NsUnit layout");
 constexpr int kNsUStaged = 1;       // u read from staging
 constexpr int kNsVStaged = 2;       // v written to staging
 constexpr int kNsTransposed = 4;    // rows > cols: X = u^T
+constexpr int kNsFuse = 8;          // local unit whose rows are whole MX blocks: the
+                                    // fused update applies f2 and G in the last epilogue
 
 // A Newton-Schulz shape class: units with the same (m, n) = (min, max) of
 // (rows, cols).  X is stored padded to mp x np (mp multiple of 128, np
@@ -94,18 +97,27 @@ struct GemmParams {
     int32_t sym;              // symmetric output: write (i, j) and (j, i) for j >= i only
     int32_t group_m;          // tile-rows per raster band of the full grid (0 = 8)
     int32_t inject_no_ready;  // failure test: never signal an accumulator as ready
+    // fused update (last iteration): w <- w*decay - step*v and G for kNsFuse units
+    int32_t fuse;
+    int32_t has_decay;
+    float decay;
+    float* w_root;
+    uint8_t* q_root;
+    uint8_t* s_root;
 };
 
 // ---- launchers (return cudaGetLastError() of the launch) -----------------
 int device_sm_count();
 int32_t* device_error_word();
 
-cudaError_t launch_f0(const RangeArgs& ra, float* m, const float* g, uint16_t* u, float mu,
-                      int nesterov, cudaStream_t st);
+cudaError_t launch_f0(const RangeArgs& ra, float* m, const float* g, uint16_t* u, uint16_t* u_stage,
+                      float mu, int nesterov, cudaStream_t st);
 cudaError_t launch_copy_bf16(const RangeArgs& ra, const uint16_t* src, uint16_t* dst, cudaStream_t st);
 cudaError_t launch_f2(const RangeArgs& ra, float* w, const float* v_root, const float* v_stage,
                       float decay, int has_decay, cudaStream_t st);
 cudaError_t launch_requant(const RangeArgs& ra, const float* w, uint8_t* q, uint8_t* s, cudaStream_t st);
+cudaError_t launch_f2_requant(const RangeArgs& ra, float* w, const float* v_root, const float* v_stage,
+                              uint8_t* q, uint8_t* s, float decay, int has_decay, cudaStream_t st);
 cudaError_t launch_adamw(float* w, const void* g, int g_bf16, float* m, float* v, int64_t n,
                          float lr, float beta1, float beta2, float eps, float decay,
                          float step_size, float inv_sqrt_bc2, cudaStream_t st);

@@ -126,6 +126,73 @@ def test_muon_variants_nesterov_decay_alpha(hm, dev):
     s.close()
 
 
+def _logical_v(hm, s, cfg):
+    v = s.fetch("v").numpy()
+    for i, un in enumerate(cfg.units):
+        if not hm.muon_plan_unit(s.plan, i)["local"]:
+            v[un.offset:un.offset + un.numel] = s.staging(i)[1].cpu().numpy()
+    return v
+
+
+@pytest.mark.parametrize("name,variant", [("tiny", "plain"), ("tiny_ragged", "plain"), ("mixed", "plain"),
+                                          ("mixed", "decay_alpha"), ("moe_small", "plain")])
+def test_fused_update_equals_unfused(hm, dev, name, variant):
+    """HM_STAGE_ALL_FUSED (gather folded into f0; f2 and G in the last
+    Newton-Schulz epilogue) gives bit-identical m, u, w, q, s to the unfused
+    stages, over two consecutive updates; its w is f2 of the unfused v."""
+    if name == "moe_small":
+        cfg = workloads.scaled_muon("moe_small", [(256, 384, None)] * 6 + [(384, 256, None)] * 3, so=8, sw=4, sg=4)
+        cfg.edge_shift = workloads.ragged_shift(8, 300, seed=5)
+    else:
+        cfg = workloads.get(name)
+    if variant == "decay_alpha":
+        cfg.muon = dataclasses.replace(cfg.muon, weight_decay=0.1, alpha_mode=2, lr=float(np.float32(0.02)))
+    data = workloads.generate(cfg, seed=17)
+    grads = [data["g"], workloads.gaussian(cfg.numel, cfg.g_std, seed=19)]
+    m0 = workloads.gaussian(cfg.numel, 1e-3, seed=18)
+    results = {}
+    for stages in (hm.HM_STAGE_ALL, hm.HM_STAGE_ALL_FUSED):
+        s = _session(cfg, dev)
+        s.load("w", data["w"])
+        s.load("m", m0)
+        per_step = []
+        for g in grads:
+            s.load("g", g)
+            s.run(_hp(cfg.muon), stages)
+            torch.cuda.synchronize()
+            out = {k: s.fetch(k).numpy() for k in ("m", "u", "w", "q", "s")}
+            if stages == hm.HM_STAGE_ALL:
+                out["v"] = _logical_v(hm, s, cfg)
+            per_step.append(out)
+        assert all(s.canary_intact().values())
+        assert hm.hm_device_error() == 0
+        results[stages] = per_step
+        s.close()
+    w_prev = data["w"]
+    for ref, got in zip(results[hm.HM_STAGE_ALL], results[hm.HM_STAGE_ALL_FUSED]):
+        for k in ("m", "u", "w", "q", "s"):
+            a, b = ref[k], got[k]
+            if a.dtype == np.float32:
+                a, b = a.view(np.uint32), b.view(np.uint32)
+            assert np.array_equal(a, b), f"fused {k} differs"
+        check_f2(cfg, w_prev, ref["v"], got["w"], cfg.muon)
+        check_requant(cfg, got["w"], got["q"], got["s"])
+        w_prev = got["w"]
+
+
+def test_fused_stage_sets_are_validated(hm, dev):
+    import ctypes as C
+    cfg = workloads.get("tiny")
+    s = _session(cfg, dev)
+    hp = _hp(cfg.muon)
+    for bad in (hm.HM_STAGE_F0 | hm.HM_STAGE_FUSED, hm.HM_STAGE_NS | hm.HM_STAGE_FUSED,
+                hm.HM_STAGE_NS | hm.HM_STAGE_F2 | hm.HM_STAGE_FUSED):
+        st = hm.lib().muon_update_units(C.c_void_p(s.plan), C.byref(s.bufs), C.byref(hp), C.c_void_p(s.ws),
+                                        s.ws_bytes, bad, None)
+        assert st == hm.HM_ERR_ARG
+    s.close()
+
+
 def test_muon_zero_gradient_unit_and_lr_zero(hm, dev):
     cfg = workloads.get("tiny_ragged")
     data = workloads.generate(cfg, seed=16)
