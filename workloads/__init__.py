@@ -259,7 +259,6 @@ def mixed() -> Config:
     for e in range(3):
         b.add(f"e{e}", 192, 320)                 # m = 192 -> padded to 256
     b.add("odd", 96, 160)                        # n = 160 -> padded to 192
-    b.add("narrow", 64, 48)                      # rows not whole 1x32 blocks (48 columns)
     return Config("mixed", "test mix of unit shapes over 8 ragged ranks", "muon", b.members, b.units,
                   so=8, sw=4, sg=4, edge_shift=ragged_shift(8, 400, seed=8))
 
