@@ -338,7 +338,9 @@ __device__ __forceinline__ void fused_f2_requant(const GemmParams& p, const NsUn
     const int lane = threadIdx.x & 31;
     const int64_t o = nu.v_off;
     if (!(nu.flags & kNsTransposed)) {
-        // stored rows = X rows (m_real), stored cols = n_real (a multiple of 32)
+        // stored rows = X rows (m_real), stored cols = n_real (a multiple of 32);
+        // chunks in the zero padding of X (n_real <= j0 < np) hold no weights
+        if (j0 >= p.n_real) return;  // warp-uniform
         const int cols = p.n_real;
         float* wrow = p.w_root + o + j0;
 #pragma unroll 8
