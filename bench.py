@@ -3,8 +3,10 @@ batched Newton-Schulz, scatter + f2, MXFP8 requant) on one GB300 per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
-One step = one call of muon_update_units over the whole workload (all five
-stages), inputs resident in HBM.  Prints one JSON line on rank 0.  Under
+One step = one update phase over the whole workload through
+muon_update_units with the fused stages (f0 + gather; Newton-Schulz with f2 and
+MXFP8 requant in its last epilogue), inputs resident in HBM; an unfused
+stage-by-stage pass afterwards gives the per-kernel HBM table.  Prints one JSON line on rank 0.  Under
 torchrun each rank runs an independent replica on its own GPU (the path has
 no cross-GPU exchange on one box): whole-job params/s = ranks * P * K / max
 over ranks of the timed region.
@@ -268,21 +270,21 @@ def run_ours(args, cfg):
     hp = muon_hparams(cfg.muon)
     stream = torch.cuda.Stream(device=dev)
     info = sess.info
-    launches_per_step = (1 + (1 if info.n_straddling else 0) + info.n_classes * (3 + 3 * cfg.muon.ns_steps) + 2)
+    front = abi.HM_STAGE_F0 | abi.HM_STAGE_GATHER | abi.HM_STAGE_FUSED
+    back = abi.HM_STAGE_NS | abi.HM_STAGE_F2 | abi.HM_STAGE_REQUANT | abi.HM_STAGE_FUSED
+    launches_per_step = 1 + info.n_classes * (3 + 3 * cfg.muon.ns_steps) + (1 if info.n_straddling else 0)
 
     def step(ev=None):
+        """One update phase, fused: f0 with the gather folded in, then
+        Newton-Schulz with f2 and MXFP8 requant in its last epilogue."""
         if ev is None:
-            sess.run(hp, abi.HM_STAGE_ALL, stream)
+            sess.run(hp, abi.HM_STAGE_ALL_FUSED, stream)
             return
         ev[0].record(stream)
-        sess.run(hp, abi.HM_STAGE_F0 | abi.HM_STAGE_GATHER, stream)
+        sess.run(hp, front, stream)
         ev[1].record(stream)
-        sess.run(hp, abi.HM_STAGE_NS, stream)
+        sess.run(hp, back, stream)
         ev[2].record(stream)
-        sess.run(hp, abi.HM_STAGE_F2, stream)
-        ev[3].record(stream)
-        sess.run(hp, abi.HM_STAGE_REQUANT, stream)
-        ev[4].record(stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -291,7 +293,7 @@ def run_ours(args, cfg):
     if abi.hm_device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -309,15 +311,25 @@ def run_ours(args, cfg):
         dist.barrier()
     clocks.stop()
     ms = t_begin.elapsed_time(t_end)
-    stage_ms = {"f0_gather": [], "ns": [], "f2": [], "requant": []}
-    for e in evs:
-        stage_ms["f0_gather"].append(e[0].elapsed_time(e[1]))
-        stage_ms["ns"].append(e[1].elapsed_time(e[2]))
-        stage_ms["f2"].append(e[2].elapsed_time(e[3]))
-        stage_ms["requant"].append(e[3].elapsed_time(e[4]))
-    stage_ms = {k: statistics.mean(v) for k, v in stage_ms.items()}
+    stage_ms = {"f0_gather": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+                "ns_f2_requant": statistics.mean(e[1].elapsed_time(e[2]) for e in evs)}
     if abi.hm_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
+
+    # per-kernel breakdown: the unfused stages, one call each, CUDA events between
+    # them (a separate, shorter timed loop after the headline one)
+    n_unfused = min(3, args.steps)
+    uev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_unfused)]
+    with torch.cuda.stream(stream):
+        for e in uev:
+            e[0].record(stream)
+            for j, st_flag in enumerate((abi.HM_STAGE_F0, abi.HM_STAGE_GATHER, abi.HM_STAGE_NS, abi.HM_STAGE_F2,
+                                         abi.HM_STAGE_REQUANT)):
+                sess.run(hp, st_flag, stream)
+                e[j + 1].record(stream)
+    torch.cuda.synchronize()
+    unfused_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in uev)
+                  for j, name in enumerate(("f0", "gather", "ns", "f2", "requant"))}
 
     if dist:
         t = torch.tensor([ms], device=dev)
@@ -342,7 +354,7 @@ def run_ours(args, cfg):
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
             sess.g.copy_(g_host, non_blocking=True)
-            sess.run(hp, abi.HM_STAGE_ALL, stream)
+            sess.run(hp, abi.HM_STAGE_ALL_FUSED, stream)
             q_host.copy_(sess.q, non_blocking=True)
             s_host.copy_(sess.s, non_blocking=True)
         e1.record(stream)
@@ -363,28 +375,33 @@ def run_ours(args, cfg):
 
     peaks = load_peaks()
     flops = ns_flops(cfg, cfg.muon.ns_steps)
-    ns_tflops = flops / (stage_ms["ns"] / 1e3) / 1e12
+    ns_tflops = flops / (stage_ms["ns_f2_requant"] / 1e3) / 1e12
     exec_flops = ns_executed_flops(cfg, cfg.muon.ns_steps)
-    exec_tflops = exec_flops / (stage_ms["ns"] / 1e3) / 1e12
+    exec_tflops = exec_flops / (stage_ms["ns_f2_requant"] / 1e3) / 1e12
     P = cfg.numel
     strad = straddling_elems(cfg, info)
-    bytes_f0 = 14.0 * P + 4.0 * strad
-    bytes_f2 = 12.0 * P
-    bytes_rq = 5.03125 * P
     kern = {
-        "f0_gather": {"gbs": bytes_f0 / (stage_ms["f0_gather"] / 1e3) / 1e9},
-        "f2_scatter": {"gbs": bytes_f2 / (stage_ms["f2"] / 1e3) / 1e9},
-        "mxfp8_requant": {"gbs": bytes_rq / (stage_ms["requant"] / 1e3) / 1e9},
+        "f0": {"gbs": 14.0 * P / (unfused_ms["f0"] / 1e3) / 1e9, "bytes_per_elem": 14},
+        "gather": {"gbs": 4.0 * strad / (unfused_ms["gather"] / 1e3) / 1e9 if strad else None,
+                   "bytes_per_straddling_elem": 4},
+        "f2_scatter": {"gbs": 12.0 * P / (unfused_ms["f2"] / 1e3) / 1e9, "bytes_per_elem": 12},
+        "mxfp8_requant": {"gbs": 5.03125 * P / (unfused_ms["requant"] / 1e3) / 1e9, "bytes_per_elem": 5.03125},
+        "f0_gather_fused": {"gbs": (14.0 * P + 2.0 * strad) / (stage_ms["f0_gather"] / 1e3) / 1e9,
+                            "bytes_per_elem": "14 + 2 per straddling element"},
     }
     for k in kern:
-        kern[k]["frac"] = kern[k]["gbs"] / peaks["hbm_gbs"]
+        if kern[k]["gbs"] is not None:
+            kern[k]["frac"] = kern[k]["gbs"] / peaks["hbm_gbs"]
+    kern["ns_unfused"] = {"tflops": flops / (unfused_ms["ns"] / 1e3) / 1e12, "ms": unfused_ms["ns"],
+                          "frac": flops / (unfused_ms["ns"] / 1e3) / 1e12 / peaks["bf16_sustained"]}
     if adamw:
         kern["adamw_flat_64M"] = adamw
         adamw["frac"] = adamw["gbs"] / peaks["hbm_gbs"]
     roofline = {"bound": "tensor", "achieved": ns_tflops, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                 "frac": ns_tflops / peaks["bf16_sustained"], "traffic": ns_stage_traffic(cfg),
-                "traffic_unit": "DRAM bytes per Newton-Schulz stage (one update), ncu",
-                "kernel": "Newton-Schulz stage (ns_gemm_kernel, 15 launches per shape class, plus norm/prepare)",
+                "traffic_unit": "DRAM bytes per fused Newton-Schulz + f2 + MXFP8 pass (one update), ncu",
+                "kernel": "fused Newton-Schulz pass: ns_gemm_kernel (15 launches per shape class, f2 + MXFP8 "
+                          "requant in the last epilogue) + norm/prepare + f2_requant for straddling fragments",
                 "peak_kind": f"bf16 dense sustained ({peaks['source']})",
                 "frac_of_burst": ns_tflops / peaks["bf16"],
                 "note": "achieved counts the algorithmic 5(4m^2n+2m^3) FLOP per unit; the kernels skip the "
@@ -408,7 +425,8 @@ def run_ours(args, cfg):
                            "emulated_ranks": cfg.so, "parallelism": f"replica x{world}",
                            "l2": "inputs larger than L2 (resident state ~%.0f GB)" % (
                                (sess.total * 21 + sess.ws_bytes) / 1e9)},
-                "ns_tflops": ns_tflops, "ns_flops_per_step": flops, "ns_executed_flops_per_step": exec_flops, "stages_ms": stage_ms, "kernels": kern,
+                "ns_tflops": ns_tflops, "ns_flops_per_step": flops, "ns_executed_flops_per_step": exec_flops,
+                "stages_ms": stage_ms, "unfused_stages_ms": unfused_ms, "kernels": kern,
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "steps": e2e_steps},
