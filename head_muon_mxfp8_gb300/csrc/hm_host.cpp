@@ -340,17 +340,12 @@ struct hm_muon_plan {
     std::vector<UnitPlan> up;
     std::vector<NsClassDev> classes;
     std::vector<NsUnit> ns_units;
-    int n_fused = 0;
     std::vector<Range> seg_tab, gather_tab;
     mutable std::vector<Range> f2_tab;
     std::vector<std::pair<int, int>> f2_shape;  // (rows, cols) of each f2 entry's unit
-    // fused update: f0 with the gather folded in, and f2 + G for the units the
-    // last Newton-Schulz epilogue does not update in place
+    // fused update: f0 with the gather folded in (f2 + G reuse the f2 table)
     std::vector<Range> f0x_tab;
-    mutable std::vector<Range> f2q_tab;
-    std::vector<std::pair<int, int>> f2q_shape;
-    mutable std::vector<NsUnit> ns_units_dev;   // ns_units with the per-unit step filled in
-    size_t off_f0x = 0, off_f2q = 0;
+    size_t off_f0x = 0;
     int64_t staging_elems = 0;
     int n_straddling = 0, n_frag = 0;
     size_t off_seg = 0, off_gather = 0, off_f2 = 0, off_nsu = 0, off_ustage = 0, off_vstage = 0;
@@ -446,12 +441,6 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
             nu.v_off = nu.u_off;
             nu.flags = (q.local ? 0 : (hm::kNsUStaged | hm::kNsVStaged)) |
                        (u.rows > u.cols ? hm::kNsTransposed : 0);
-            // the fused update quantizes in the epilogue: every stored row of
-            // the unit must be whole 1x32 MX blocks, and the unit must be local
-            if (q.local && u.cols % HM_MX_BLOCK == 0) {
-                nu.flags |= hm::kNsFuse;
-                p->n_fused++;
-            }
             p->ns_units.push_back(nu);
         }
         p->classes.push_back(c);
@@ -489,12 +478,13 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
                     continue;
                 }
             }
-            p->f2_tab.push_back(Range{f.root_offset, f.root_offset, 0, f.length, pre, 0.f, 0});
+            p->f2_tab.push_back(Range{f.root_offset, f.root_offset, f.root_offset, f.length, pre, 0.f, 0});
             p->f2_shape.push_back({u.rows, u.cols});
             pre += f.length;
         } else {
             for (const hm_fragment& f : q.frags) {
-                p->f2_tab.push_back(Range{f.root_offset, q.stage_off + f.unit_offset, 0, f.length, pre, 0.f, 1});
+                p->f2_tab.push_back(Range{f.root_offset, q.stage_off + f.unit_offset, f.root_offset, f.length, pre,
+                                          0.f, 1});
                 p->f2_shape.push_back({u.rows, u.cols});
                 pre += f.length;
             }
@@ -519,19 +509,6 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
             pre += f.length;
         }
     }
-    pre = 0;
-    for (int i = 0; i < n_units; ++i) {
-        const hm_unit_desc& u = units[i];
-        const UnitPlan& q = p->up[i];
-        if (q.local && u.cols % HM_MX_BLOCK == 0) continue;  // updated in the last epilogue
-        for (const hm_fragment& f : q.frags) {
-            p->f2q_tab.push_back(Range{f.root_offset, q.local ? f.root_offset : q.stage_off + f.unit_offset,
-                                       f.root_offset, f.length, pre, 0.f, q.local ? 0 : 1});
-            p->f2q_shape.push_back({u.rows, u.cols});
-            pre += f.length;
-        }
-    }
-    p->ns_units_dev = p->ns_units;
 
     // workspace layout (every region 1024-byte aligned)
     size_t off = 0;
@@ -545,7 +522,6 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
     p->off_f2 = take(p->f2_tab.size() * sizeof(Range));
     p->off_nsu = take(p->ns_units.size() * sizeof(NsUnit));
     p->off_f0x = take(p->f0x_tab.size() * sizeof(Range));
-    p->off_f2q = take(p->f2q_tab.size() * sizeof(Range));
     p->off_ustage = take(static_cast<size_t>(p->staging_elems) * 2);
     p->off_vstage = take(static_cast<size_t>(p->staging_elems) * 4);
     for (NsClassDev& c : p->classes) {
@@ -647,7 +623,7 @@ extern "C" hm_status muon_plan_upload(hm_muon_plan* p, void* workspace, size_t w
     };
     if (put(p->off_seg, p->seg_tab.data(), p->seg_tab.size() * sizeof(Range)) != cudaSuccess ||
         put(p->off_gather, p->gather_tab.data(), p->gather_tab.size() * sizeof(Range)) != cudaSuccess ||
-        put(p->off_nsu, p->ns_units_dev.data(), p->ns_units_dev.size() * sizeof(NsUnit)) != cudaSuccess)
+        put(p->off_nsu, p->ns_units.data(), p->ns_units.size() * sizeof(NsUnit)) != cudaSuccess)
         return HM_ERR_CUDA;
     for (size_t k = 0; k < p->classes.size(); ++k)
         if (put(p->classes[k].sym_off, p->sym_tab[k].data(), p->sym_tab[k].size() * 4) != cudaSuccess)
@@ -688,24 +664,15 @@ extern "C" hm_status muon_plan_staging(const hm_muon_plan* p, int unit, uint16_t
 
 namespace {
 
-// Per-unit steps fp32(lr * alpha) live in the f2, f2+G and Newton-Schulz unit
-// tables; they are rewritten (and re-uploaded, stream-ordered) whenever lr or
-// the alpha mode changes.
+// Per-unit steps fp32(lr * alpha) live in the f2 table; it is rewritten (and
+// re-uploaded, stream-ordered) whenever lr or the alpha mode changes.
 hm_status refresh_steps(const hm_muon_plan* p, const hm_muon_hparams* hp, cudaStream_t s) {
     if (hp->lr == p->f2_lr && hp->alpha_mode == p->f2_alpha_mode) return HM_OK;
-    auto step = [&](int rows, int cols) {
-        return static_cast<float>(static_cast<double>(hp->lr) * alpha_of(hp->alpha_mode, rows, cols));
-    };
-    for (size_t i = 0; i < p->f2_tab.size(); ++i) p->f2_tab[i].step = step(p->f2_shape[i].first, p->f2_shape[i].second);
-    for (size_t i = 0; i < p->f2q_tab.size(); ++i)
-        p->f2q_tab[i].step = step(p->f2q_shape[i].first, p->f2q_shape[i].second);
-    for (NsUnit& nu : p->ns_units_dev) nu.step = step(nu.rows, nu.cols);
-    auto put = [&](size_t off, const void* src, size_t bytes) {
-        return bytes == 0 ? cudaSuccess : cudaMemcpyAsync(p->ws + off, src, bytes, cudaMemcpyHostToDevice, s);
-    };
-    if (put(p->off_f2, p->f2_tab.data(), p->f2_tab.size() * sizeof(Range)) != cudaSuccess ||
-        put(p->off_f2q, p->f2q_tab.data(), p->f2q_tab.size() * sizeof(Range)) != cudaSuccess ||
-        put(p->off_nsu, p->ns_units_dev.data(), p->ns_units_dev.size() * sizeof(NsUnit)) != cudaSuccess)
+    for (size_t i = 0; i < p->f2_tab.size(); ++i)
+        p->f2_tab[i].step = static_cast<float>(static_cast<double>(hp->lr) *
+                                               alpha_of(hp->alpha_mode, p->f2_shape[i].first, p->f2_shape[i].second));
+    if (!p->f2_tab.empty() && cudaMemcpyAsync(p->ws + p->off_f2, p->f2_tab.data(), p->f2_tab.size() * sizeof(Range),
+                                              cudaMemcpyHostToDevice, s) != cudaSuccess)
         return HM_ERR_CUDA;
     p->f2_lr = hp->lr;
     p->f2_alpha_mode = hp->alpha_mode;
@@ -719,11 +686,11 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
     if (!p || !b || !hp || stages < 0 || stages > (HM_STAGE_ALL | HM_STAGE_FUSED)) return HM_ERR_ARG;
     const bool fused = stages & HM_STAGE_FUSED;
     if (fused) {
-        // the fused passes cross stage boundaries: f0 + gather, and NS + f2 + G
+        // the fused passes cross stage boundaries: f0 + gather, and f2 + G
         const int front = stages & (HM_STAGE_F0 | HM_STAGE_GATHER);
-        const int back = stages & (HM_STAGE_NS | HM_STAGE_F2 | HM_STAGE_REQUANT);
+        const int back = stages & (HM_STAGE_F2 | HM_STAGE_REQUANT);
         if ((front && front != (HM_STAGE_F0 | HM_STAGE_GATHER)) ||
-            (back && back != (HM_STAGE_NS | HM_STAGE_F2 | HM_STAGE_REQUANT)))
+            (back && back != (HM_STAGE_F2 | HM_STAGE_REQUANT)))
             return HM_ERR_ARG;
     }
     if (!p->ws) return HM_ERR_STATE;
@@ -744,7 +711,7 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
     uint16_t* u_stage = reinterpret_cast<uint16_t*>(ws + p->off_ustage);
     float* v_stage = reinterpret_cast<float*>(ws + p->off_vstage);
 
-    if ((stages & (HM_STAGE_F2 | HM_STAGE_NS)) && (st = refresh_steps(p, hp, s)) != HM_OK) return st;
+    if ((stages & HM_STAGE_F2) && (st = refresh_steps(p, hp, s)) != HM_OK) return st;
     if (fused && (stages & HM_STAGE_F0)) {
         // f0 writes u of straddling fragments into their staging as well
         RangeArgs ra = device_ranges(ws, p->off_f0x, p->f0x_tab);
@@ -806,23 +773,15 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g3.m_real = c.m; g3.n_real = c.n;
                 g3.group_m = c.mp / 128;  // column bands: each X panel is fetched once per unit
                 g3.err = g1.err;
-                if (fused && last) {
-                    g3.fuse = 1;
-                    g3.w_root = b->w;
-                    g3.q_root = b->q;
-                    g3.s_root = b->s;
-                    g3.decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
-                    g3.has_decay = hp->weight_decay != 0.f;
-                }
                 if (hm::launch_ns_gemm(mp.b_a, mp.x_mn[cur], g3, mp.bn3, 1, s) != cudaSuccess) return HM_ERR_CUDA;
                 cur ^= 1;
             }
         }
     }
     if (fused && (stages & HM_STAGE_F2)) {
-        // f2 + G for the fragments whose v went through memory
-        if (!p->f2q_tab.empty()) {
-            RangeArgs ra = device_ranges(ws, p->off_f2q, p->f2q_tab);
+        // f2 and G in one pass: the new w of every element is quantized as it is written
+        if (!p->f2_tab.empty()) {
+            RangeArgs ra = device_ranges(ws, p->off_f2, p->f2_tab);
             const float decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
             if (hm::launch_f2_requant(ra, b->w, b->v, v_stage, b->q, b->s, decay, hp->weight_decay != 0.f, s) !=
                 cudaSuccess)

@@ -48,14 +48,12 @@ struct NsUnit {
     int32_t rows;    // unit as stored: rows x cols, row-major
     int32_t cols;
     int32_t flags;   // kNs* bits
-    float step;      // fp32(lr * alpha) of the unit (fused f2)
+    int32_t pad;
 };
 static_assert(sizeof(NsUnit) == 32, "NsUnit layout");
 constexpr int kNsUStaged = 1;       // u read from staging
 constexpr int kNsVStaged = 2;       // v written to staging
 constexpr int kNsTransposed = 4;    // rows > cols: X = u^T
-constexpr int kNsFuse = 8;          // local unit whose rows are whole MX blocks: the
-                                    // fused update applies f2 and G in the last epilogue
 
 // A Newton-Schulz shape class: units with the same (m, n) = (min, max) of
 // (rows, cols).  X is stored padded to mp x np (mp multiple of 128, np
@@ -97,13 +95,6 @@ struct GemmParams {
     int32_t sym;              // symmetric output: write (i, j) and (j, i) for j >= i only
     int32_t group_m;          // tile-rows per raster band of the full grid (0 = 8)
     int32_t inject_no_ready;  // failure test: never signal an accumulator as ready
-    // fused update (last iteration): w <- w*decay - step*v and G for kNsFuse units
-    int32_t fuse;
-    int32_t has_decay;
-    float decay;
-    float* w_root;
-    uint8_t* q_root;
-    uint8_t* s_root;
 };
 
 // ---- launchers (return cudaGetLastError() of the launch) -----------------

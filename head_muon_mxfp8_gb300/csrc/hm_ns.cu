@@ -31,7 +31,6 @@
 // records HM_ERR_TIMEOUT in the device error word, lets every role finish,
 // waits for its own TMA copies and MMAs, frees TMEM and returns.
 #include "hm_internal.h"
-#include "hm_mx_device.cuh"
 
 #include <cuda_bf16.h>
 
@@ -321,84 +320,6 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& x, float* f) {
 }
 __device__ __forceinline__ uint32_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
-// Fused update of one 32 x 32 block of a kNsFuse unit in the last epilogue:
-// v (this lane's 32 values of row i of X) never goes to memory; the lane's
-// main-weight elements get f2, w <- w*decay - step*v (the same fp32 operations
-// as the f2 kernel), and the new weights are quantized to MXFP8 in place.
-// MX blocks run along the stored rows of the unit: for a non-transposed unit
-// they are this lane's 32 values, for a transposed one they are the 32 lanes
-// of the warp at a fixed column.
-__device__ __forceinline__ float f2_op(float w, float v, float step, float decay, int has_decay) {
-    const float a = has_decay ? __fmul_rn(w, decay) : w;
-    return __fsub_rn(a, __fmul_rn(step, v));
-}
-
-__device__ __forceinline__ void fused_f2_requant(const GemmParams& p, const NsUnit& nu, int i, int i0, int j0,
-                                                 const float (&v)[32], float* stage) {
-    const int lane = threadIdx.x & 31;
-    const int64_t o = nu.v_off;
-    if (!(nu.flags & kNsTransposed)) {
-        // stored rows = X rows (m_real), stored cols = n_real (a multiple of 32);
-        // chunks in the zero padding of X (n_real <= j0 < np) hold no weights
-        if (j0 >= p.n_real) return;  // warp-uniform
-        const int cols = p.n_real;
-        float* wrow = p.w_root + o + j0;
-#pragma unroll 8
-        for (int r2 = 0; r2 < 32; ++r2)
-            if (i0 + r2 < p.m_real) stage[r2 * 33 + lane] = wrow[static_cast<int64_t>(i0 + r2) * cols + lane];
-        __syncwarp();
-        if (i < p.m_real) {
-            float x[32];
-            float amax = 0.f;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                x[k] = f2_op(stage[lane * 33 + k], v[k], nu.step, p.decay, p.has_decay);
-                amax = fmaxf(amax, fabsf(x[k]));
-                stage[lane * 33 + k] = x[k];
-            }
-            const int e = mx_scale_exponent(amax);
-            const float sc = mx_inv_scale(e);
-            uint32_t c[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                c[k] = cvt_e4m3x2(x[4 * k] * sc, x[4 * k + 1] * sc) |
-                       (static_cast<uint32_t>(cvt_e4m3x2(x[4 * k + 2] * sc, x[4 * k + 3] * sc)) << 16);
-            const int64_t e0 = o + static_cast<int64_t>(i) * cols + j0;
-            uint4* qp = reinterpret_cast<uint4*>(p.q_root + e0);
-            qp[0] = make_uint4(c[0], c[1], c[2], c[3]);
-            qp[1] = make_uint4(c[4], c[5], c[6], c[7]);
-            p.s_root[e0 >> 5] = static_cast<uint8_t>(e + 127);
-        }
-        __syncwarp();
-#pragma unroll 8
-        for (int r2 = 0; r2 < 32; ++r2)
-            if (i0 + r2 < p.m_real) wrow[static_cast<int64_t>(i0 + r2) * cols + lane] = stage[r2 * 33 + lane];
-        __syncwarp();
-    } else {
-        // stored rows = X columns (n_real), stored cols = m_real (a multiple of 32):
-        // X(i, j) is w[j][i]; at a fixed j the warp's 32 lanes hold one MX block
-        if (i0 >= p.m_real) return;  // warp-uniform
-        const int cols = p.m_real;
-        float wv[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-            wv[k] = (j0 + k < p.n_real) ? p.w_root[o + static_cast<int64_t>(j0 + k) * cols + i] : 0.f;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            if (j0 + k >= p.n_real) continue;  // warp-uniform
-            const float x = f2_op(wv[k], v[k], nu.step, p.decay, p.has_decay);
-            float amax = fabsf(x);
-#pragma unroll
-            for (int sh = 16; sh; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
-            const int e = mx_scale_exponent(amax);
-            const int64_t idx = o + static_cast<int64_t>(j0 + k) * cols + i;
-            p.w_root[idx] = x;
-            p.q_root[idx] = static_cast<uint8_t>(cvt_e4m3x2(x * mx_inv_scale(e), 0.f) & 0xFFu);
-            if (lane == 0) p.s_root[(idx) >> 5] = static_cast<uint8_t>(e + 127);
-        }
-    }
-}
-
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm, int tn, int row, uint32_t taddr,
                                               float* stage) {
@@ -428,10 +349,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm
         }
         if (p.epi == kEpiFinal) {
             const NsUnit nu = p.ns_units[u];
-            if (p.fuse && (nu.flags & kNsFuse)) {
-                fused_f2_requant(p, nu, i, i0, j0, v, stage);
-                continue;
-            }
             if (i < p.m_real && (nu.flags & kNsTransposed)) {
                 float* dst = ((nu.flags & kNsVStaged) ? p.v_stage : p.v_root) + nu.v_off;
                 {

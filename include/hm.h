@@ -201,14 +201,13 @@ typedef struct {  /* device roots, each in the chain's emulated layout */
 #define HM_STAGE_F2      8   /* v fragments -> owners; w <- w - lr alpha v  */
 #define HM_STAGE_REQUANT 16  /* G: w -> (q, s) in every segment             */
 #define HM_STAGE_ALL     31
-/* Fused update (SS-HSDP section 4.2 "Fully Zero Copy"): with HM_STAGE_FUSED,
- * F0 and GATHER run as one pass (f0 also writes the u fragments of straddling
- * units into their staging), and NS, F2 and REQUANT run as one pass: the last
- * Newton-Schulz epilogue applies f2 and G in place to every local unit whose
- * stored rows are whole 1x32 blocks, so their v is never written; one
- * f2 + G pass then covers the fragments of the other units.  F0 and GATHER
- * must be requested together, and NS, F2 and REQUANT together (else
- * HM_ERR_ARG).  Outputs m, u, w, q, s equal those of the unfused stages. */
+/* Fused update (SS-HSDP section 4.2 "Fully Zero Copy": no extra copies):
+ * with HM_STAGE_FUSED, F0 and GATHER run as one pass (f0 also writes the u
+ * fragments of straddling units into their staging, so u is read once), and
+ * F2 and REQUANT run as one pass (w is read once; its new value is quantized
+ * as it is written).  F0 and GATHER must be requested together, and F2 and
+ * REQUANT together (else HM_ERR_ARG); NS runs as usual.  Outputs m, u, v, w,
+ * q, s equal those of the unfused stages bit for bit. */
 #define HM_STAGE_FUSED   32
 #define HM_STAGE_ALL_FUSED 63
 

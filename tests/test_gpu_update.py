@@ -137,9 +137,9 @@ def _logical_v(hm, s, cfg):
 @pytest.mark.parametrize("name,variant", [("tiny", "plain"), ("tiny_ragged", "plain"), ("mixed", "plain"),
                                           ("mixed", "decay_alpha"), ("moe_small", "plain")])
 def test_fused_update_equals_unfused(hm, dev, name, variant):
-    """HM_STAGE_ALL_FUSED (gather folded into f0; f2 and G in the last
-    Newton-Schulz epilogue) gives bit-identical m, u, w, q, s to the unfused
-    stages, over two consecutive updates; its w is f2 of the unfused v."""
+    """HM_STAGE_ALL_FUSED (gather folded into f0; f2 and G in one pass) gives
+    bit-identical m, u, v, w, q, s to the unfused stages, over two
+    consecutive updates; its w is f2 of the unfused v."""
     if name == "moe_small":
         cfg = workloads.scaled_muon("moe_small", [(256, 384, None)] * 6 + [(384, 256, None)] * 3, so=8, sw=4, sg=4)
         cfg.edge_shift = workloads.ragged_shift(8, 300, seed=5)
@@ -161,8 +161,7 @@ def test_fused_update_equals_unfused(hm, dev, name, variant):
             s.run(_hp(cfg.muon), stages)
             torch.cuda.synchronize()
             out = {k: s.fetch(k).numpy() for k in ("m", "u", "w", "q", "s")}
-            if stages == hm.HM_STAGE_ALL:
-                out["v"] = _logical_v(hm, s, cfg)
+            out["v"] = _logical_v(hm, s, cfg)
             per_step.append(out)
         assert all(s.canary_intact().values())
         assert hm.hm_device_error() == 0
@@ -170,7 +169,7 @@ def test_fused_update_equals_unfused(hm, dev, name, variant):
         s.close()
     w_prev = data["w"]
     for ref, got in zip(results[hm.HM_STAGE_ALL], results[hm.HM_STAGE_ALL_FUSED]):
-        for k in ("m", "u", "w", "q", "s"):
+        for k in ("m", "u", "v", "w", "q", "s"):
             a, b = ref[k], got[k]
             if a.dtype == np.float32:
                 a, b = a.view(np.uint32), b.view(np.uint32)
@@ -185,8 +184,8 @@ def test_fused_stage_sets_are_validated(hm, dev):
     cfg = workloads.get("tiny")
     s = _session(cfg, dev)
     hp = _hp(cfg.muon)
-    for bad in (hm.HM_STAGE_F0 | hm.HM_STAGE_FUSED, hm.HM_STAGE_NS | hm.HM_STAGE_FUSED,
-                hm.HM_STAGE_NS | hm.HM_STAGE_F2 | hm.HM_STAGE_FUSED):
+    for bad in (hm.HM_STAGE_F0 | hm.HM_STAGE_FUSED, hm.HM_STAGE_GATHER | hm.HM_STAGE_FUSED,
+                hm.HM_STAGE_NS | hm.HM_STAGE_F2 | hm.HM_STAGE_FUSED, hm.HM_STAGE_REQUANT | hm.HM_STAGE_FUSED):
         st = hm.lib().muon_update_units(C.c_void_p(s.plan), C.byref(s.bufs), C.byref(hp), C.c_void_p(s.ws),
                                         s.ws_bytes, bad, None)
         assert st == hm.HM_ERR_ARG
