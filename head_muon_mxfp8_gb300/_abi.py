@@ -79,6 +79,11 @@ class hm_mx_tensor(C.Structure):
                 ("rows", C.c_int64), ("k", C.c_int64)]
 
 
+class hm_scale_relayout(C.Structure):
+    _fields_ = [("src_offset", C.c_int64), ("dst_offset", C.c_int64), ("rows", C.c_int64), ("kb", C.c_int64),
+                ("block_rows", C.c_int32), ("pad", C.c_int32)]
+
+
 class HmError(RuntimeError):
     def __init__(self, fn: str, status: int):
         super().__init__(f"{fn} returned {status} ({status_str(status)})")
@@ -112,6 +117,8 @@ _SIGS = {
     "muon_plan_destroy": (None, [_P]),
     "adamw_update_flat": (C.c_int, [_P, _P, C.c_int, _P, _P, C.c_int64, C.POINTER(hm_adamw_hparams), _P]),
     "mxfp8_requant_packed": (C.c_int, [_P, _P, _P, C.POINTER(hm_mx_tensor), C.c_int, _P]),
+    "mxfp8_requant_32x32": (C.c_int, [_P, _P, _P, _P, C.POINTER(hm_mx_tensor), C.c_int, _P]),
+    "mxfp8_scale_relayout": (C.c_int, [_P, _P, C.POINTER(hm_scale_relayout), C.c_int, _P]),
     "newton_schulz_noalloc": (C.c_int, [_P, C.c_int32, C.c_int32, _P, C.POINTER(hm_muon_hparams), _P]),
 }
 
@@ -270,6 +277,18 @@ def mxfp8_requant_packed(w: int, q: int, scales: int, tensors, stream: int = 0) 
     arr = (hm_mx_tensor * max(1, len(tensors)))(*[hm_mx_tensor(*t) for t in tensors])
     check("mxfp8_requant_packed", lib().mxfp8_requant_packed(_P(w), _P(q), _P(scales), arr, len(tensors),
                                                              _P(stream)))
+
+
+def mxfp8_requant_32x32(chain: int, w: int, q: int, scales: int, tensors, stream: int = 0) -> None:
+    arr = (hm_mx_tensor * max(1, len(tensors)))(*[hm_mx_tensor(*t) for t in tensors])
+    check("mxfp8_requant_32x32", lib().mxfp8_requant_32x32(_P(chain), _P(w), _P(q), _P(scales), arr, len(tensors),
+                                                           _P(stream)))
+
+
+def mxfp8_scale_relayout(src: int, dst: int, items, stream: int = 0) -> None:
+    """items: (src_offset, dst_offset, rows, kb, block_rows)."""
+    arr = (hm_scale_relayout * max(1, len(items)))(*[hm_scale_relayout(*it, 0) for it in items])
+    check("mxfp8_scale_relayout", lib().mxfp8_scale_relayout(_P(src), _P(dst), arr, len(items), _P(stream)))
 
 
 def newton_schulz_noalloc(u: int, rows: int, cols: int, v: int, hp: hm_muon_hparams, stream: int = 0) -> None:

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhm.so")
 
-SOURCES = ["hm_host.cpp", "hm_elementwise.cu", "hm_ns.cu", "hm_noalloc.cu"]
+SOURCES = ["hm_host.cpp", "hm_elementwise.cu", "hm_ns.cu", "hm_noalloc.cu", "hm_mx32.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "-I" + INCLUDE, "-I" + CSRC]

@@ -857,3 +857,80 @@ extern "C" hm_status mxfp8_requant_packed(const float* w, uint8_t* q, uint8_t* s
     }
     return HM_OK;
 }
+
+// ============================================================================
+// G with 32 x 32 blocks and Tw's scale relayout (EG1; section 4.1)
+// ============================================================================
+extern "C" hm_status mxfp8_requant_32x32(const hm_chain* chain, const float* w, uint8_t* q, uint8_t* scales,
+                                         const hm_mx_tensor* tensors, int n, void* stream) {
+    if (n < 0 || (n > 0 && !tensors)) return HM_ERR_ARG;
+    if (n == 0) return HM_OK;
+    if (!w || !q || !scales) return HM_ERR_ARG;
+    if (chain && chain->so > hm::kMaxChainRanks) return HM_ERR_ARG;
+    for (int i = 0; i < n; ++i) {
+        const hm_mx_tensor& t = tensors[i];
+        if (t.rows < 0 || t.k < 0 || t.src_offset < 0 || t.scale_offset < 0) return HM_ERR_ARG;
+        if (t.rows % HM_MX_BLOCK || t.k % HM_MX_BLOCK || t.src_offset % HM_MX_BLOCK) return HM_ERR_ALIGN;
+        if (chain && t.src_offset + t.rows * t.k > chain->n) return HM_ERR_GEOMETRY;
+    }
+    hm_status st = check_arch();
+    if (st != HM_OK) return st;
+    hm::ChainArgs ch;
+    std::memset(&ch, 0, sizeof(ch));
+    if (chain) {
+        ch.so = chain->so;
+        for (int c = 0; c <= chain->so; ++c) ch.edges[c] = chain->edges[c];
+        for (int c = 0; c < chain->so; ++c) ch.chunk_base[c] = chain->base[chain->owner[c]];
+    }
+    for (int g0 = 0; g0 < n; g0 += hm::kMaxMx32Tensors) {
+        hm::Mx32Args ta;
+        std::memset(&ta, 0, sizeof(ta));
+        for (int i = g0; i < n && i < g0 + hm::kMaxMx32Tensors; ++i) {
+            const hm_mx_tensor& t = tensors[i];
+            if (!t.rows || !t.k) continue;
+            ta.src[ta.n] = t.src_offset;
+            ta.k[ta.n] = t.k;
+            ta.scale_off[ta.n] = t.scale_offset;
+            ta.block_prefix[ta.n + 1] = ta.block_prefix[ta.n] + (t.rows / 32) * (t.k / 32);
+            ta.n++;
+        }
+        if (!ta.n) continue;
+        if (hm::launch_requant_32x32(ch, ta, w, q, scales, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return HM_ERR_CUDA;
+    }
+    return HM_OK;
+}
+
+extern "C" hm_status mxfp8_scale_relayout(const uint8_t* src, uint8_t* dst, const hm_scale_relayout* items, int n,
+                                          void* stream) {
+    if (n < 0 || (n > 0 && !items)) return HM_ERR_ARG;
+    if (n == 0) return HM_OK;
+    if (!src || !dst) return HM_ERR_ARG;
+    for (int i = 0; i < n; ++i) {
+        const hm_scale_relayout& it = items[i];
+        if (it.rows < 0 || it.kb < 0 || it.src_offset < 0 || it.dst_offset < 0) return HM_ERR_ARG;
+        if (it.block_rows != 1 && it.block_rows != 32) return HM_ERR_ARG;
+        if (it.rows % it.block_rows) return HM_ERR_ALIGN;
+    }
+    hm_status st = check_arch();
+    if (st != HM_OK) return st;
+    for (int g0 = 0; g0 < n; g0 += hm::kMaxRelayoutItems) {
+        hm::RelayoutArgs ra;
+        std::memset(&ra, 0, sizeof(ra));
+        for (int i = g0; i < n && i < g0 + hm::kMaxRelayoutItems; ++i) {
+            const hm_scale_relayout& it = items[i];
+            if (!it.rows || !it.kb) continue;
+            ra.src[ra.n] = it.src_offset;
+            ra.dst[ra.n] = it.dst_offset;
+            ra.rows[ra.n] = it.rows;
+            ra.kb[ra.n] = it.kb;
+            ra.block_rows[ra.n] = it.block_rows;
+            ra.out_prefix[ra.n + 1] = ra.out_prefix[ra.n] + ((it.rows + 127) / 128) * ((it.kb + 3) / 4) * 512;
+            ra.n++;
+        }
+        if (!ra.n) continue;
+        if (hm::launch_scale_relayout(ra, src, dst, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return HM_ERR_CUDA;
+    }
+    return HM_OK;
+}

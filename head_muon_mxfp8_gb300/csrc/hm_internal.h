@@ -97,6 +97,37 @@ struct GemmParams {
     int32_t inject_no_ready;  // failure test: never signal an accumulator as ready
 };
 
+// chain geometry the device needs: z1 edges and the segment base of every chunk
+constexpr int kMaxChainRanks = 256;
+struct ChainArgs {
+    int32_t so;          // 0: flat, logical == root
+    int32_t pad;
+    int64_t edges[kMaxChainRanks + 1];
+    int64_t chunk_base[kMaxChainRanks];
+};
+
+constexpr int kMaxMx32Tensors = 32;
+struct Mx32Args {
+    int32_t n;
+    int32_t pad;
+    int64_t block_prefix[kMaxMx32Tensors + 1];  // exclusive prefix of 32x32 block counts
+    int64_t src[kMaxMx32Tensors];
+    int64_t k[kMaxMx32Tensors];
+    int64_t scale_off[kMaxMx32Tensors];
+};
+
+constexpr int kMaxRelayoutItems = 32;
+struct RelayoutArgs {
+    int32_t n;
+    int32_t pad;
+    int64_t out_prefix[kMaxRelayoutItems + 1];  // exclusive prefix of output bytes
+    int64_t src[kMaxRelayoutItems];
+    int64_t dst[kMaxRelayoutItems];
+    int64_t rows[kMaxRelayoutItems];
+    int64_t kb[kMaxRelayoutItems];
+    int32_t block_rows[kMaxRelayoutItems];
+};
+
 // ---- launchers (return cudaGetLastError() of the launch) -----------------
 int device_sm_count();
 int32_t* device_error_word();
@@ -112,6 +143,10 @@ cudaError_t launch_f2_requant(const RangeArgs& ra, float* w, const float* v_root
 cudaError_t launch_adamw(float* w, const void* g, int g_bf16, float* m, float* v, int64_t n,
                          float lr, float beta1, float beta2, float eps, float decay,
                          float step_size, float inv_sqrt_bc2, cudaStream_t st);
+
+cudaError_t launch_requant_32x32(const ChainArgs& ch, const Mx32Args& ta, const float* w, uint8_t* q,
+                                 uint8_t* scales, cudaStream_t st);
+cudaError_t launch_scale_relayout(const RelayoutArgs& ra, const uint8_t* src, uint8_t* dst, cudaStream_t st);
 
 cudaError_t launch_ns_norm(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
                            const uint16_t* u_stage, char* ws, float eps, cudaStream_t st);

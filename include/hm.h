@@ -286,6 +286,45 @@ hm_status mxfp8_requant_packed(const float* w, uint8_t* q, uint8_t* scales,
 hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int32_t cols, float* v,
                                 const hm_muon_hparams* hp, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* G with 32 x 32 blocks (section 3.1 EG1: "32 x 32 block quantization in a
+ * k-major layout"): one UE8M0 scale per 32-row x 32-column block of each
+ * [rows][K] tensor, e = clamp(floor(log2 amax) - 8, -127, 127) over the 1024
+ * elements, elements E4M3 RNE saturated.  A block spans 32 rows, so it can
+ * straddle ZeRO-1 edges: with a chain, w and q are emulated roots in the
+ * chain's layout and every block row is read from (and written to) the rank
+ * segment that holds it -- the in-HBM form of gathering the block to an
+ * execution rank.  chain == NULL: w and q are flat, logical order.
+ * tensors[i]: src_offset = logical element offset of the tensor (a multiple
+ * of 32), rows and k multiples of 32 (else HM_ERR_ALIGN), scale_offset = byte
+ * offset of its [rows/32][k/32] scale matrix in `scales`; dst_offset is not
+ * used (codes land at each element's own position in q).  At most 256 ranks
+ * (HM_ERR_ARG).  n = 0 is a no-op. */
+hm_status mxfp8_requant_32x32(const hm_chain* chain, const float* w, uint8_t* q, uint8_t* scales,
+                              const hm_mx_tensor* tensors, int n, void* stream);
+
+/* Tw's scale relayout (EG1: scales are relaid out for the GEMM kernel;
+ * section 4.1: batched across tensors).  Each item takes a K-major scale
+ * matrix [rows / block_rows][kb] (block_rows 1 for 1 x 32 blocks, 32 for
+ * 32 x 32 blocks, whose scale is repeated over its 32 rows) at src + src_offset
+ * and writes the 128 x 4 tiled layout read by block-scaled tensor-core GEMMs
+ * (the cuBLAS "1D block scaling factors" layout) at dst + dst_offset:
+ * ceil(rows/128) * ceil(kb/4) tiles of 512 bytes, tile (i, j) at
+ * (i * ceil(kb/4) + j) * 512, row r / column c of a tile at
+ * (r % 32) * 16 + (r / 32) * 4 + c, padding zero.  rows % block_rows == 0
+ * (HM_ERR_ALIGN).  n = 0 is a no-op. */
+typedef struct {
+    int64_t src_offset;   /* bytes */
+    int64_t dst_offset;   /* bytes */
+    int64_t rows;         /* weight rows */
+    int64_t kb;           /* scales per row = K / 32 */
+    int32_t block_rows;   /* 1 or 32 */
+    int32_t pad;
+} hm_scale_relayout;
+
+hm_status mxfp8_scale_relayout(const uint8_t* src, uint8_t* dst, const hm_scale_relayout* items, int n,
+                               void* stream);
+
 #ifdef __cplusplus
 }
 #endif

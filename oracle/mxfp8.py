@@ -133,3 +133,51 @@ def dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     vals = np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
     scale = np.ldexp(1.0, s.astype(np.int64) - SCALE_BIAS)
     return vals[q] * np.repeat(scale, BLOCK)
+
+
+# ---------------------------------------------------------------------------
+# 32 x 32 blocks (section 3.1 EG1: "32 x 32 block quantization in a k-major
+# layout") and the kernel-facing scale layout of Tw.
+# ---------------------------------------------------------------------------
+def quantize_tensor_32x32(w: np.ndarray):
+    """[rows][K] float32 -> (codes [rows][K], scales [rows/32][K/32]); one
+    UE8M0 scale per 32 x 32 block, same exponent rule and element rounding as
+    the 1 x 32 case, the block amax taken over all 1024 elements."""
+    w = np.asarray(w, dtype=np.float32)
+    rows, k = w.shape
+    if rows % BLOCK or k % BLOCK:
+        raise ValueError("rows and K must be multiples of 32")
+    blocks = w.reshape(rows // BLOCK, BLOCK, k // BLOCK, BLOCK).astype(np.float64)
+    amax = np.abs(blocks).max(axis=(1, 3))
+    e = np.full(amax.shape, -127, dtype=np.int64)
+    nz = amax > 0
+    _, kexp = np.frexp(amax[nz])
+    e[nz] = np.clip(kexp.astype(np.int64) - 1 - E4M3_EMAX, -127, 127)
+    y = blocks * np.ldexp(1.0, -e)[:, None, :, None]
+    codes = e4m3_encode(y).reshape(rows, k)
+    return codes, (e + SCALE_BIAS).astype(np.uint8)
+
+
+def scale_tile_128x4(sf: np.ndarray) -> np.ndarray:
+    """Row-wise scale matrix sf [rows][kb] (kb = K/32 scales per row) ->
+    the 128 x 4 tiled layout that block-scaled tensor-core GEMMs read
+    (cuBLAS documentation, "1D block scaling factors layout"): rows and kb are
+    padded with zeros to multiples of 128 and 4; tile (i, j) of 128 rows x 4
+    scale columns occupies 512 bytes at (i * ceil(kb/4) + j) * 512, and inside
+    a tile, row r and column c sit at (r % 32) * 16 + (r // 32) * 4 + c."""
+    sf = np.asarray(sf, dtype=np.uint8)
+    rows, kb = sf.shape
+    rt, ct = -(-rows // 128), -(-kb // 4)
+    out = np.zeros(rt * ct * 512, dtype=np.uint8)
+    for r in range(rows):
+        for c in range(kb):
+            tile = (r // 128) * ct + c // 4
+            rr, cc = r % 128, c % 4
+            out[tile * 512 + (rr % 32) * 16 + (rr // 32) * 4 + cc] = sf[r, c]
+    return out
+
+
+def expand_block_rows(sf32: np.ndarray, block_rows: int = BLOCK) -> np.ndarray:
+    """Scales of 32 x 32 blocks [rows/32][kb] -> one row per weight row
+    [rows][kb] (each block's scale repeated over its 32 rows)."""
+    return np.repeat(np.asarray(sf32, dtype=np.uint8), block_rows, axis=0)

@@ -115,3 +115,49 @@ def test_power_of_two_multiples_of_codes_are_exact():
     expect = (codes | sign).astype(np.uint8)
     assert (q == expect).all()
     assert (s.astype(np.int64) - 127 == k).all()
+
+
+def test_32x32_scale_is_the_max_of_its_row_block_scales():
+    """floor(log2) and the clamp are monotone, so a 32 x 32 block's exponent is
+    the largest of its 32 row-block (1 x 32) exponents; elements then use the
+    same encoder with that exponent."""
+    rng = np.random.default_rng(11)
+    w = (rng.standard_normal((96, 128)) * 0.02).astype(np.float32)
+    w[:32, :32] *= np.float32(1e-6)                       # a block of tiny magnitude
+    w[32:64, 64:96] = 0.0                                 # an all-zero block
+    w[70, 100] = np.float32(3e4)                          # one outlier dominates its block
+    c32, s32 = MX.quantize_tensor_32x32(w)
+    c1, s1 = MX.quantize_tensor(w)
+    assert (s32 == s1.reshape(3, 32, 4).max(axis=1)).all()
+    e = s32.astype(np.int64) - 127
+    for bi in range(3):
+        for bj in range(4):
+            blk = w[32 * bi:32 * bi + 32, 32 * bj:32 * bj + 32].astype(np.float64)
+            want = MX.e4m3_encode(blk * np.ldexp(1.0, -e[bi, bj])).reshape(32, 32)
+            assert (c32[32 * bi:32 * bi + 32, 32 * bj:32 * bj + 32] == want).all()
+    assert s32[1, 2] == 0 and (c32[32:64, 64:96] == 0).all()
+
+
+def test_scale_tile_128x4_structure():
+    """The 128 x 4 tiled scale layout is a permutation of the padded scale
+    matrix; each 512-byte tile holds exactly its 128 x 4 sub-block; inside a
+    tile, the 16 bytes at 16 * l are rows l, l + 32, l + 64, l + 96 (4 scale
+    columns each) - the 32-row interleave a 32-lane warp reads as one row per
+    lane."""
+    rng = np.random.default_rng(12)
+    rows, kb = 256, 8
+    sf = rng.integers(0, 255, size=(rows, kb)).astype(np.uint8)
+    out = MX.scale_tile_128x4(sf)
+    assert out.size == rows * kb and sorted(out.tolist()) == sorted(sf.ravel().tolist())
+    ct = kb // 4
+    for ti in range(rows // 128):
+        for tj in range(ct):
+            tile = out[(ti * ct + tj) * 512:(ti * ct + tj + 1) * 512]
+            sub = sf[128 * ti:128 * ti + 128, 4 * tj:4 * tj + 4]
+            assert sorted(tile.tolist()) == sorted(sub.ravel().tolist())
+            for lane in range(32):
+                grp = tile[16 * lane:16 * lane + 16].reshape(4, 4)
+                assert (grp == sub[[lane, lane + 32, lane + 64, lane + 96], :]).all()
+    # ragged sizes are zero-padded to whole tiles
+    small = MX.scale_tile_128x4(np.full((5, 3), 7, np.uint8))
+    assert small.size == 512 and int((small == 7).sum()) == 15
