@@ -41,6 +41,7 @@ HM_STAGE_REQUANT = 16
 HM_STAGE_ALL = 31
 HM_STAGE_FUSED = 32
 HM_STAGE_ALL_FUSED = 63
+HM_RS_FP32, HM_RS_BF16, HM_RS_BF16_SR = 0, 1, 2
 
 
 class hm_fragment(C.Structure):
@@ -119,6 +120,8 @@ _SIGS = {
     "mxfp8_requant_packed": (C.c_int, [_P, _P, _P, C.POINTER(hm_mx_tensor), C.c_int, _P]),
     "mxfp8_requant_32x32": (C.c_int, [_P, _P, _P, _P, C.POINTER(hm_mx_tensor), C.c_int, _P]),
     "mxfp8_scale_relayout": (C.c_int, [_P, _P, C.POINTER(hm_scale_relayout), C.c_int, _P]),
+    "reduce_scatter_grad": (C.c_int, [_P, _P, C.c_int, C.c_int, _P, C.c_int, C.c_int, C.c_uint64, C.c_uint64,
+                                      _P]),
     "newton_schulz_noalloc": (C.c_int, [_P, C.c_int32, C.c_int32, _P, C.POINTER(hm_muon_hparams), _P]),
 }
 
@@ -289,6 +292,12 @@ def mxfp8_scale_relayout(src: int, dst: int, items, stream: int = 0) -> None:
     """items: (src_offset, dst_offset, rows, kb, block_rows)."""
     arr = (hm_scale_relayout * max(1, len(items)))(*[hm_scale_relayout(*it, 0) for it in items])
     check("mxfp8_scale_relayout", lib().mxfp8_scale_relayout(_P(src), _P(dst), arr, len(items), _P(stream)))
+
+
+def reduce_scatter_grad(chain: int, parts: int, n_parts: int, ranks_per_node: int, g: int, mode: int,
+                        accumulate: bool, seed: int, offset: int, stream: int = 0) -> None:
+    check("reduce_scatter_grad", lib().reduce_scatter_grad(_P(chain), _P(parts), n_parts, ranks_per_node, _P(g), mode,
+                                                           int(accumulate), seed, offset, _P(stream)))
 
 
 def newton_schulz_noalloc(u: int, rows: int, cols: int, v: int, hp: hm_muon_hparams, stream: int = 0) -> None:

@@ -253,6 +253,77 @@ __global__ void __launch_bounds__(kThreads) f2_requant_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
+// Outer reduce-scatter of the gradient with FP32 / BF16 / BF16-SR node partials.
+// Range r covers rank segment r: root offset r.a, logical start r.b.
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of two 32x32
+// multiplies with the published multipliers and key increments; returns
+// output word 0.
+__device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                                 uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return c0;
+}
+
+__device__ __forceinline__ float round_partial(float s, int mode, int64_t i, int node, const RsArgs& a) {
+    if (mode == 1) return __bfloat162float(__float2bfloat16_rn(s));
+    if (mode == 2) {
+        const uint32_t r = philox_word0(static_cast<uint32_t>(i), static_cast<uint32_t>(static_cast<uint64_t>(i) >> 32),
+                                        static_cast<uint32_t>(node), a.offset_lo, a.seed_lo, a.seed_hi) & 0xFFFFu;
+        return __uint_as_float(((__float_as_uint(s) + r) >> 16) << 16);
+    }
+    return s;
+}
+
+__global__ void __launch_bounds__(kThreads) reduce_scatter_kernel(const __grid_constant__ RangeArgs ra,
+                                                                  const __grid_constant__ RsArgs a,
+                                                                  float* __restrict__ g) {
+    const int nodes = a.n_parts / a.ranks_per_node;
+    for (int64_t t0 = blockIdx.x * kTile; t0 < ra.total; t0 += static_cast<int64_t>(gridDim.x) * kTile) {
+        int ri = find_range(ra, t0);
+        const int64_t t1 = min(t0 + kTile, ra.total);
+        for (int64_t v = t0 + threadIdx.x * 4; v < t1; v += kThreads * 4) {
+            while (v >= range_at(ra, ri).prefix + range_at(ra, ri).len) ++ri;
+            const Range& r = range_at(ra, ri);
+            const int64_t d = v - r.prefix;
+            const int64_t i = r.b + d;  // logical element index
+            float tot[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k < nodes; ++k) {
+                float s[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int l = 0; l < a.ranks_per_node; ++l) {
+                    const float4 x = __ldcs(reinterpret_cast<const float4*>(
+                        a.parts + static_cast<int64_t>(k * a.ranks_per_node + l) * a.stride + i));
+                    s[0] = __fadd_rn(s[0], x.x); s[1] = __fadd_rn(s[1], x.y);
+                    s[2] = __fadd_rn(s[2], x.z); s[3] = __fadd_rn(s[3], x.w);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) tot[e] = __fadd_rn(tot[e], round_partial(s[e], a.mode, i + e, k, a));
+            }
+            float4* gp = reinterpret_cast<float4*>(g + r.a + d);
+            if (a.accumulate) {
+                const float4 o = *gp;
+                tot[0] = __fadd_rn(o.x, tot[0]); tot[1] = __fadd_rn(o.y, tot[1]);
+                tot[2] = __fadd_rn(o.z, tot[2]); tot[3] = __fadd_rn(o.w, tot[3]);
+            }
+            *gp = make_float4(tot[0], tot[1], tot[2], tot[3]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // AdamW (decoupled weight decay, bias-corrected), 4 elements per thread step;
 // the scalar tail (n % 4) is handled by the first threads of block 0.
 // ---------------------------------------------------------------------------
@@ -362,6 +433,12 @@ cudaError_t launch_f2_requant(const RangeArgs& ra, float* w, const float* v_root
                               uint8_t* s, float decay, int has_decay, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
     f2_requant_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, w, v_root, v_stage, q, s, decay, has_decay);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_scatter(const RangeArgs& ra, const RsArgs& a, float* g, cudaStream_t st) {
+    if (ra.total == 0) return cudaSuccess;
+    reduce_scatter_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, a, g);
     return cudaGetLastError();
 }
 

@@ -934,3 +934,43 @@ extern "C" hm_status mxfp8_scale_relayout(const uint8_t* src, uint8_t* dst, cons
     }
     return HM_OK;
 }
+
+// ============================================================================
+// Outer reduce-scatter of the gradient (sections 3.4 and 4.3; Table 4)
+// ============================================================================
+extern "C" hm_status reduce_scatter_grad(const hm_chain* chain, const float* parts, int n_parts, int ranks_per_node,
+                                         float* g, int mode, int accumulate, uint64_t seed, uint64_t offset,
+                                         void* stream) {
+    if (!chain || n_parts < 1 || ranks_per_node < 1) return HM_ERR_ARG;
+    if (mode < HM_RS_FP32 || mode > HM_RS_BF16_SR) return HM_ERR_ARG;
+    if (n_parts % ranks_per_node) return HM_ERR_GEOMETRY;
+    if (chain->n == 0) return HM_OK;
+    if (!parts || !g) return HM_ERR_ARG;
+    if (!aligned16(parts) || !aligned16(g)) return HM_ERR_ALIGN;
+    hm_status st = check_arch();
+    if (st != HM_OK) return st;
+    hm::RsArgs a{};
+    a.parts = parts;
+    a.stride = chain->n;
+    a.n_parts = n_parts;
+    a.ranks_per_node = ranks_per_node;
+    a.mode = mode;
+    a.accumulate = accumulate ? 1 : 0;
+    a.seed_lo = static_cast<uint32_t>(seed);
+    a.seed_hi = static_cast<uint32_t>(seed >> 32);
+    a.offset_lo = static_cast<uint32_t>(offset);
+    for (int r0 = 0; r0 < chain->so; r0 += hm::kInlineRanges) {
+        RangeArgs ra;
+        std::memset(&ra, 0, sizeof(ra));
+        int64_t pre = 0;
+        for (int r = r0; r < chain->so && r < r0 + hm::kInlineRanges; ++r) {
+            if (!chain->len[r]) continue;
+            ra.inl[ra.n++] = Range{chain->base[r], chain->edges[chain->chunk_of[r]], 0, chain->len[r], pre, 0.f, 0};
+            pre += chain->len[r];
+        }
+        ra.total = pre;
+        if (!ra.n) continue;
+        if (hm::launch_reduce_scatter(ra, a, g, static_cast<cudaStream_t>(stream)) != cudaSuccess) return HM_ERR_CUDA;
+    }
+    return HM_OK;
+}

@@ -148,6 +148,14 @@ cudaError_t launch_requant_32x32(const ChainArgs& ch, const Mx32Args& ta, const 
                                  uint8_t* scales, cudaStream_t st);
 cudaError_t launch_scale_relayout(const RelayoutArgs& ra, const uint8_t* src, uint8_t* dst, cudaStream_t st);
 
+struct RsArgs {
+    const float* parts;
+    int64_t stride;      // elements per contribution row (= n)
+    int32_t n_parts, ranks_per_node, mode, accumulate;
+    uint32_t seed_lo, seed_hi, offset_lo, pad;
+};
+cudaError_t launch_reduce_scatter(const RangeArgs& ra, const RsArgs& a, float* g, cudaStream_t st);
+
 cudaError_t launch_ns_norm(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
                            const uint16_t* u_stage, char* ws, float eps, cudaStream_t st);
 cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,

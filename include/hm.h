@@ -325,6 +325,35 @@ typedef struct {
 hm_status mxfp8_scale_relayout(const uint8_t* src, uint8_t* dst, const hm_scale_relayout* items, int n,
                                void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Outer reduce-scatter of the main gradient, emulated in HBM (section 3.4
+ * Update: Tg maps the accumulated gradients to the update representation and
+ * the outer reduce-scatter produces the ZeRO-1 main-gradient shards; section
+ * 4.3 ZeroSM reduce-scatter: intra-node FP32 reduce, inter-node exchange,
+ * final FP32 reduce accumulating into the persistent gradient; node-local
+ * partials optionally BF16 with stochastic rounding; Table 4: the SR seed /
+ * counter state is restored on the same logical rank).
+ *
+ * parts: device, n_parts x n fp32, row p = contribution of rank p in logical
+ * order (n = the chain's tensor-list length); ranks form nodes of
+ * ranks_per_node consecutive rows.  g: device root in the chain's layout.
+ * For every element i (written in the rank segment that owns it):
+ *   s_k   = fp32 sum of the node's rows, in row order
+ *   p_k   = s_k (HM_RS_FP32) | bf16_RNE(s_k) (HM_RS_BF16) |
+ *           bf16_SR(s_k) (HM_RS_BF16_SR: 16 random bits added to the low half
+ *           of the fp32 pattern, then truncated; bits = low 16 bits of word 0
+ *           of Philox4x32-10, counter (i mod 2^32, i div 2^32, k, offset mod
+ *           2^32), key (seed mod 2^32, seed div 2^32))
+ *   total = fp32 sum of the p_k in node order
+ *   g     = accumulate ? g + total : total
+ * Rejects n_parts not a multiple of ranks_per_node (HM_ERR_GEOMETRY), a bad
+ * mode (HM_ERR_ARG), pointers not 16-byte aligned (HM_ERR_ALIGN). */
+#define HM_RS_FP32    0
+#define HM_RS_BF16    1
+#define HM_RS_BF16_SR 2
+hm_status reduce_scatter_grad(const hm_chain* chain, const float* parts, int n_parts, int ranks_per_node,
+                              float* g, int mode, int accumulate, uint64_t seed, uint64_t offset, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
