@@ -371,6 +371,9 @@ def run_ours(args, cfg):
     h2d = sess.total * 4
     d2h = sess.total + sess.total // 32
 
+    # ---- the NEXT-row kernels on the same workload (their own timed loops) --
+    extra = {} if args.skip_extra else bench_next_rows(cfg, sess, dev, stream)
+
     # ---- AdamW on the flat 64M shard (its own small timed loop) ----------
     adamw = None
     if not args.skip_adamw:
@@ -402,6 +405,9 @@ def run_ours(args, cfg):
     if adamw:
         kern["adamw_flat_64M"] = adamw
         adamw["frac"] = adamw["gbs"] / peaks["hbm_gbs"]
+    for k, v in extra.items():
+        v["frac"] = v["gbs"] / peaks["hbm_gbs"]
+        kern[k] = v
     roofline = {"bound": "tensor", "achieved": ns_tflops, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                 "frac": ns_tflops / peaks["bf16_sustained"], "traffic": ns_stage_traffic(cfg),
                 "traffic_unit": "DRAM bytes per Newton-Schulz stage (one update), ncu",
@@ -440,6 +446,63 @@ def run_ours(args, cfg):
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def _time_calls(fn, stream, reps: int = 3):
+    import torch
+    with torch.cuda.stream(stream):
+        fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def bench_next_rows(cfg, sess, dev, stream):
+    """32 x 32 MXFP8 requant over the rank segments, the 128 x 4 scale relayout
+    of every tensor's 1 x 32 scales, and the emulated gradient reduce-scatter
+    (4 contributions in 2 nodes, BF16 stochastic rounding, accumulate), each
+    timed with CUDA events on the bench stream."""
+    import torch
+
+    from head_muon_mxfp8_gb300 import abi
+    sh = int(stream.cuda_stream)
+    P = cfg.numel
+    out = {}
+    tensors, s_off = [], 0
+    for m in cfg.members:
+        tensors.append((m.offset, 0, s_off, m.rows, m.cols))
+        s_off += (m.rows // 32) * (m.cols // 32)
+    sc32 = torch.empty(s_off, dtype=torch.uint8, device=dev)
+    ms = _time_calls(lambda: abi.mxfp8_requant_32x32(sess.chain, sess.w.data_ptr(), sess.q.data_ptr(),
+                                                     sc32.data_ptr(), tensors, sh), stream)
+    out["mxfp8_requant_32x32"] = {"gbs": 5.0 * P / (ms / 1e3) / 1e9, "ms": ms, "bytes_per_elem": 5}
+    items, src_off, dst_off = [], 0, 0
+    for m in cfg.members:
+        kb = m.cols // 32
+        items.append((src_off, dst_off, m.rows, kb, 1))
+        src_off += m.rows * kb
+        dst_off += -(-m.rows // 128) * -(-kb // 4) * 512
+    src = torch.zeros(src_off, dtype=torch.uint8, device=dev)
+    dst = torch.empty(dst_off, dtype=torch.uint8, device=dev)
+    ms = _time_calls(lambda: abi.mxfp8_scale_relayout(src.data_ptr(), dst.data_ptr(), items, sh), stream)
+    out["mxfp8_scale_relayout"] = {"gbs": (src_off + dst_off) / (ms / 1e3) / 1e9, "ms": ms,
+                                   "bytes": "scales read + tiled scales written"}
+    del src, dst, sc32
+    parts = torch.empty((4, P), dtype=torch.float32, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    parts.normal_(0.0, 1e-3, generator=gen)
+    ms = _time_calls(lambda: abi.reduce_scatter_grad(sess.chain, parts.data_ptr(), 4, 2, sess.g.data_ptr(),
+                                                     abi.HM_RS_BF16_SR, True, 1234, 0, sh), stream)
+    out["grad_reduce_scatter_bf16sr"] = {"gbs": 24.0 * P / (ms / 1e3) / 1e9, "ms": ms,
+                                         "bytes_per_elem": "4 contributions x 4 + g read and written"}
+    del parts
+    return out
 
 
 def bench_adamw(dev, stream, steps: int = 10):
@@ -481,6 +544,7 @@ def main():
     ap.add_argument("--workload", default="video_dit", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-adamw", action="store_true")
+    ap.add_argument("--skip-extra", action="store_true", help="skip the 32x32 / relayout / reduce-scatter timings")
     args = ap.parse_args()
     cfg = workloads.get(args.workload)
     if cfg.optimizer != "muon":
