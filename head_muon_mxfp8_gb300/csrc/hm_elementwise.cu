@@ -257,10 +257,9 @@ __global__ void __launch_bounds__(kThreads) f2_requant_kernel(const __grid_const
 // Range r covers rank segment r: root offset r.a, logical start r.b.
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of two 32x32
-// multiplies with the published multipliers and key increments; returns
-// output word 0.
-__device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
-                                                 uint32_t k1) {
+// multiplies with the published multipliers and key increments.
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                               uint32_t k1) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
         if (r) {
@@ -275,19 +274,11 @@ __device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint3
         c2 = n2;
         c3 = lo0;
     }
-    return c0;
+    return make_uint4(c0, c1, c2, c3);
 }
 
-__device__ __forceinline__ float round_partial(float s, int mode, int64_t i, int node, const RsArgs& a) {
-    if (mode == 1) return __bfloat162float(__float2bfloat16_rn(s));
-    if (mode == 2) {
-        const uint32_t r = philox_word0(static_cast<uint32_t>(i), static_cast<uint32_t>(static_cast<uint64_t>(i) >> 32),
-                                        static_cast<uint32_t>(node), a.offset_lo, a.seed_lo, a.seed_hi) & 0xFFFFu;
-        return __uint_as_float(((__float_as_uint(s) + r) >> 16) << 16);
-    }
-    return s;
-}
-
+// 8 elements per thread step (i a multiple of 8): one Philox call per node
+// gives the 8 16-bit stochastic-rounding fields of these elements.
 __global__ void __launch_bounds__(kThreads) reduce_scatter_kernel(const __grid_constant__ RangeArgs ra,
                                                                   const __grid_constant__ RsArgs a,
                                                                   float* __restrict__ g) {
@@ -295,30 +286,48 @@ __global__ void __launch_bounds__(kThreads) reduce_scatter_kernel(const __grid_c
     for (int64_t t0 = blockIdx.x * kTile; t0 < ra.total; t0 += static_cast<int64_t>(gridDim.x) * kTile) {
         int ri = find_range(ra, t0);
         const int64_t t1 = min(t0 + kTile, ra.total);
-        for (int64_t v = t0 + threadIdx.x * 4; v < t1; v += kThreads * 4) {
+        for (int64_t v = t0 + threadIdx.x * 8; v < t1; v += kThreads * 8) {
             while (v >= range_at(ra, ri).prefix + range_at(ra, ri).len) ++ri;
             const Range& r = range_at(ra, ri);
             const int64_t d = v - r.prefix;
-            const int64_t i = r.b + d;  // logical element index
-            float tot[4] = {0.f, 0.f, 0.f, 0.f};
+            const int64_t i = r.b + d;  // logical element index, a multiple of 8
+            float tot[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             for (int k = 0; k < nodes; ++k) {
-                float s[4] = {0.f, 0.f, 0.f, 0.f};
+                float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 for (int l = 0; l < a.ranks_per_node; ++l) {
-                    const float4 x = __ldcs(reinterpret_cast<const float4*>(
-                        a.parts + static_cast<int64_t>(k * a.ranks_per_node + l) * a.stride + i));
-                    s[0] = __fadd_rn(s[0], x.x); s[1] = __fadd_rn(s[1], x.y);
-                    s[2] = __fadd_rn(s[2], x.z); s[3] = __fadd_rn(s[3], x.w);
+                    const float4* src = reinterpret_cast<const float4*>(
+                        a.parts + static_cast<int64_t>(k * a.ranks_per_node + l) * a.stride + i);
+                    const float4 x0 = __ldcs(src), x1 = __ldcs(src + 1);
+                    const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s[e] = __fadd_rn(s[e], xv[e]);
+                }
+                if (a.mode == 1) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s[e] = __bfloat162float(__float2bfloat16_rn(s[e]));
+                } else if (a.mode == 2) {
+                    const uint64_t blk = static_cast<uint64_t>(i) >> 3;
+                    const uint4 rb = philox4x32_10(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32),
+                                                   static_cast<uint32_t>(k), a.offset_lo, a.seed_lo, a.seed_hi);
+                    const uint32_t wv[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t bits = (wv[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu;
+                        s[e] = __uint_as_float(((__float_as_uint(s[e]) + bits) >> 16) << 16);
+                    }
                 }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) tot[e] = __fadd_rn(tot[e], round_partial(s[e], a.mode, i + e, k, a));
+                for (int e = 0; e < 8; ++e) tot[e] = __fadd_rn(tot[e], s[e]);
             }
             float4* gp = reinterpret_cast<float4*>(g + r.a + d);
             if (a.accumulate) {
-                const float4 o = *gp;
-                tot[0] = __fadd_rn(o.x, tot[0]); tot[1] = __fadd_rn(o.y, tot[1]);
-                tot[2] = __fadd_rn(o.z, tot[2]); tot[3] = __fadd_rn(o.w, tot[3]);
+                const float4 o0 = gp[0], o1 = gp[1];
+                const float ov[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) tot[e] = __fadd_rn(ov[e], tot[e]);
             }
-            *gp = make_float4(tot[0], tot[1], tot[2], tot[3]);
+            gp[0] = make_float4(tot[0], tot[1], tot[2], tot[3]);
+            gp[1] = make_float4(tot[4], tot[5], tot[6], tot[7]);
         }
     }
 }

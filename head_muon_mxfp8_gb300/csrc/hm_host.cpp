@@ -891,7 +891,7 @@ extern "C" hm_status mxfp8_requant_32x32(const hm_chain* chain, const float* w, 
             ta.src[ta.n] = t.src_offset;
             ta.k[ta.n] = t.k;
             ta.scale_off[ta.n] = t.scale_offset;
-            ta.block_prefix[ta.n + 1] = ta.block_prefix[ta.n] + (t.rows / 32) * (t.k / 32);
+            ta.block_prefix[ta.n + 1] = ta.block_prefix[ta.n] + (t.rows / 32) * ((t.k + 127) / 128);  // strips
             ta.n++;
         }
         if (!ta.n) continue;

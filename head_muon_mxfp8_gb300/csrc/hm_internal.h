@@ -110,7 +110,7 @@ constexpr int kMaxMx32Tensors = 32;
 struct Mx32Args {
     int32_t n;
     int32_t pad;
-    int64_t block_prefix[kMaxMx32Tensors + 1];  // exclusive prefix of 32x32 block counts
+    int64_t block_prefix[kMaxMx32Tensors + 1];  // exclusive prefix of 32-row x 128-column strip counts
     int64_t src[kMaxMx32Tensors];
     int64_t k[kMaxMx32Tensors];
     int64_t scale_off[kMaxMx32Tensors];

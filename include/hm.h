@@ -341,9 +341,10 @@ hm_status mxfp8_scale_relayout(const uint8_t* src, uint8_t* dst, const hm_scale_
  *   s_k   = fp32 sum of the node's rows, in row order
  *   p_k   = s_k (HM_RS_FP32) | bf16_RNE(s_k) (HM_RS_BF16) |
  *           bf16_SR(s_k) (HM_RS_BF16_SR: 16 random bits added to the low half
- *           of the fp32 pattern, then truncated; bits = low 16 bits of word 0
- *           of Philox4x32-10, counter (i mod 2^32, i div 2^32, k, offset mod
- *           2^32), key (seed mod 2^32, seed div 2^32))
+ *           of the fp32 pattern, then truncated; bits = 16-bit field (i mod 8)
+ *           of the 128-bit Philox4x32-10 output for counter (i/8 mod 2^32,
+ *           i/8 div 2^32, k, offset mod 2^32) and key (seed mod 2^32, seed div
+ *           2^32); field f = bits 16*(f mod 2).. of word f/2)
  *   total = fp32 sum of the p_k in node order
  *   g     = accumulate ? g + total : total
  * Rejects n_parts not a multiple of ranks_per_node (HM_ERR_GEOMETRY), a bad

@@ -17,9 +17,10 @@ stochastically; the total is the fp32 sum of the node partials in node order;
 accumulate adds it to the existing gradient (fp32).  Stochastic rounding of
 an fp32 value to bf16 adds 16 random bits to the low half of its bit pattern
 and truncates (round up with probability equal to the discarded fraction).
-The random bits of element i and node k are the low 16 bits of the first
-word of Philox4x32-10 (Salmon et al., SC'11) with counter (i mod 2^32,
-i div 2^32, k, offset) and key (seed mod 2^32, seed div 2^32).
+The random bits of element i and node k are 16-bit field (i mod 8) of the
+128-bit output of Philox4x32-10 (Salmon et al., SC'11) with counter
+(i div 8 mod 2^32, i div 8 div 2^32, k, offset) and key (seed mod 2^32,
+seed div 2^32); field f is bits 16 (f mod 2) .. +15 of word f div 2.
 
 Pins (tests/test_oracle_gradient.py): Philox known-answer vectors
 (tests/golden/philox4x32_10_kat.txt); SR leaves bf16-representable values
@@ -57,11 +58,17 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
 
 
 def sr_bits(index, node, seed, offset):
-    """16 random bits for element `index` of node `node`."""
+    """16 random bits for element `index` of node `node`: field index mod 8 of
+    the 128-bit Philox4x32-10 output for counter (index div 8 mod 2^32,
+    index div 8 div 2^32, node, offset) and key (seed mod 2^32, seed div 2^32);
+    field f is bits 16 (f mod 2) .. 16 (f mod 2) + 15 of word f div 2."""
     index = np.asarray(index, dtype=np.uint64)
-    out = philox4x32_10(index & np.uint64(MASK), index >> np.uint64(32), np.full_like(index, node),
+    blk = index >> np.uint64(3)
+    out = philox4x32_10(blk & np.uint64(MASK), blk >> np.uint64(32), np.full_like(index, node),
                         np.full_like(index, offset & MASK), seed & MASK, (seed >> 32) & MASK)
-    return (out[0] & np.uint64(0xFFFF)).astype(np.uint32)
+    f = index & np.uint64(7)
+    word = np.choose((f >> np.uint64(1)).astype(np.int64), out)
+    return ((word >> ((f & np.uint64(1)) * np.uint64(16))) & np.uint64(0xFFFF)).astype(np.uint32)
 
 
 def bf16_sr_bits(x: np.ndarray, rbits: np.ndarray) -> np.ndarray:
