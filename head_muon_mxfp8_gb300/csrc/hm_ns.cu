@@ -25,8 +25,9 @@
 //               swizzle, STAGES-deep mbarrier ring;
 //   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=16)
 //               from one lane into a double-buffered fp32 accumulator;
-//   warps 2-5   epilogue: tcgen05.ld 32x32b rows out of TMEM, fused
-//               element-wise tail, global stores.
+//   warps 2-9   epilogue, two warps per TMEM lane quadrant, each draining
+//               half of the tile's columns: tcgen05.ld 32x32b rows out of
+//               TMEM, fused element-wise tail, global stores.
 // Every mbarrier wait is bounded (2 s of %globaltimer); on timeout the CTA
 // records HM_ERR_TIMEOUT in the device error word, lets every role finish,
 // waits for its own TMA copies and MMAs, frees TMEM and returns.
@@ -152,7 +153,8 @@ __global__ void __launch_bounds__(256) ns_prepare_kernel(const NsUnit* __restric
 // ---------------------------------------------------------------------------
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, each drains half of a tile's columns
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -278,7 +280,7 @@ struct GemmCfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int EPI_BYTES = 4 * 32 * 33 * 4;  // per epilogue warp: a 32 x 32 fp32 transpose tile
+    static constexpr int EPI_BYTES = kEpiWarps * 32 * 33 * 4;  // per epilogue warp: a 32 x 32 fp32 transpose tile
     static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + EPI_BYTES + 1024 + 256;
     // kind::f16 instruction descriptor: D fp32, A and B bf16, A K-major, B
     // K-major or (bit 16) MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
@@ -322,10 +324,10 @@ __device__ __forceinline__ uint32_t bf16_bits(float x) { return __bfloat16_as_us
 
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm, int tn, int row, uint32_t taddr,
-                                              float* stage) {
+                                              float* stage, int half) {
     const int i = tm * BM + row;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
         const int j0 = tn * BN + c * 32;
         uint32_t r[32];
         __syncwarp();
@@ -438,7 +440,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
-            mbar_init(smem_u32(&tempty[b]), 128);
+            mbar_init(smem_u32(&tempty[b]), 32 * kEpiWarps);
         }
         mbar_init(smem_u32(drain), 1);
         *bail = 0;
@@ -515,7 +517,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_wait(smem_u32(drain), 0, p.err, bail, false);
         }
     } else {
-        const int q = warp & 3;  // TMEM lane quadrant of this warp
+        const int q = warp & 3;           // TMEM lane quadrant of this warp
+        const int half = (warp - 2) >> 2;  // which half of the tile's columns it drains
         const int row = q * 32 + lane;
         int acc = 0;
         uint32_t aph = 0;
@@ -528,7 +531,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_after();
             epilogue_tile<BN>(p, u, tm, tn, row,
                               tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN),
-                              epi_stage + q * 32 * 33);
+                              epi_stage + (warp - 2) * 32 * 33, half);
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[acc]));
             acc ^= 1;
