@@ -75,7 +75,7 @@ def straddling_elems(cfg, plan_info) -> int:
 # DRAM bytes (read + write) of one Newton-Schulz stage of the Video-DiT x8
 # workload, from profiles/video_dit_launch_list_dram.md, valid for the kernel
 # source it was measured on (sha256 prefix of hm_ns.cu).
-NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 169.835e9, "hm_ns_sha256": "8b3ddd80f8956d48"}
+NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.7089e+11, "hm_ns_sha256": "d58e6666f185383b"}
 
 
 def ns_stage_traffic(cfg):
