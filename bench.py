@@ -87,6 +87,22 @@ def ns_stage_traffic(cfg):
     return NS_STAGE_TRAFFIC["bytes"]
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of one float over all ranks (a scalar, not data)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, numel: int, steps: int, ms: float) -> float:
+    """Whole-job parameters per second: every rank updates numel parameters per
+    step; the job takes the slowest rank's time."""
+    return world * numel * steps / (ms / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -334,40 +350,15 @@ def run_ours(args, cfg):
     unfused_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in uev)
                   for j, name in enumerate(("f0", "gather", "ns", "f2", "requant"))}
 
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     ms_per_step = ms / args.steps
-    value = world * cfg.numel * args.steps / (ms / 1e3)
+    value = whole_job_rate(world, cfg.numel, args.steps, ms)
 
     # ---- end to end: host gradient in, host MXFP8 runtime weight out -----
-    e2e_steps = max(1, min(3, args.steps))
-    g_host = torch.empty(sess.total, dtype=torch.float32, pin_memory=True)
-    g_host.copy_(sess.g, non_blocking=False)
-    q_host = torch.empty(sess.total, dtype=torch.uint8, pin_memory=True)
-    s_host = torch.empty(sess.total // 32, dtype=torch.uint8, pin_memory=True)
-    with torch.cuda.stream(stream):
-        for k in range(e2e_steps + 1):
-            if k == 1:
-                torch.cuda.synchronize()
-                if dist:
-                    dist.barrier()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-            sess.g.copy_(g_host, non_blocking=True)
-            sess.run(hp, abi.HM_STAGE_ALL_FUSED, stream)
-            q_host.copy_(sess.q, non_blocking=True)
-            s_host.copy_(sess.s, non_blocking=True)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * cfg.numel * e2e_steps / (e2e_ms / 1e3)
+    e2e_steps = max(2, min(4, args.steps))
+    e2e_ms = e2e_pipelined(sess, hp, stream, e2e_steps, dist)
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_value = whole_job_rate(world, cfg.numel, e2e_steps, e2e_ms)
     h2d = sess.total * 4
     d2h = sess.total + sess.total // 32
 
@@ -439,13 +430,92 @@ def run_ours(args, cfg):
                 "stages_ms": stage_ms, "unfused_stages_ms": unfused_ms, "kernels": kern,
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                        "steps": e2e_steps},
+                        "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+                        "note": "host gradient in, host MXFP8 weights + scales out, every step; copies on their own "
+                                "streams overlap the previous / next step's Newton-Schulz stage"},
                 "gpu_launches": launches_per_step * args.steps, "clocks": clocks.summary()}
         print(json.dumps(line), flush=True)
     sess.close()
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def e2e_pipelined(sess, hp, stream, steps, dist):
+    """Update phases fed from and returned to pinned host memory: every step
+    copies its gradient in (9.2 GB for Video-DiT) and its MXFP8 weights and
+    scales out.  The copies run on their own streams with double-buffered
+    device gradients, so step k+1's upload and step k's download overlap step
+    k's Newton-Schulz stage; every step's copies are inside the timed
+    region, which runs from the first upload to the last download."""
+    import torch
+
+    from head_muon_mxfp8_gb300 import abi
+    dev = sess.device
+    g_dev = [sess.g, torch.empty_like(sess.g)]
+    g_dev[1].copy_(sess.g)
+    g_host = torch.empty(sess.total, dtype=torch.float32, pin_memory=True)
+    g_host.copy_(sess.g)
+    q_host = [torch.empty(sess.total, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    s_host = [torch.empty(sess.total // 32, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    bufs = []
+    for g in g_dev:
+        b = abi.hm_muon_bufs(sess.w.data_ptr(), sess.m.data_ptr(), g.data_ptr(), sess.u.data_ptr(),
+                             sess.v.data_ptr(), sess.q.data_ptr(), sess.s.data_ptr())
+        bufs.append(b)
+    cs_in = torch.cuda.Stream(device=dev)
+    cs_out = torch.cuda.Stream(device=dev)
+    sh = int(stream.cuda_stream)
+    front = abi.HM_STAGE_F0 | abi.HM_STAGE_GATHER | abi.HM_STAGE_FUSED
+    back = abi.HM_STAGE_F2 | abi.HM_STAGE_REQUANT | abi.HM_STAGE_FUSED
+
+    def run(stages, b):
+        abi.muon_update_units(sess.plan, bufs[b], hp, sess.ws, sess.ws_bytes, stages, sh)
+
+    def pipeline(n, t0=None, t1=None):
+        ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
+        g_free = [None, None]
+        out_done = None
+        if t0 is not None:
+            t0.record(cs_in)
+        for k in range(n):
+            b = k % 2
+            in_done = ev()
+            with torch.cuda.stream(cs_in):
+                if g_free[b] is not None:
+                    cs_in.wait_event(g_free[b])
+                g_dev[b].copy_(g_host, non_blocking=True)
+                in_done.record(cs_in)
+            stream.wait_event(in_done)
+            run(front, b)
+            g_free[b] = ev()
+            g_free[b].record(stream)
+            run(abi.HM_STAGE_NS, b)
+            if out_done is not None:
+                stream.wait_event(out_done)  # the previous step's download has left q and s
+            run(back, b)
+            back_done = ev()
+            back_done.record(stream)
+            with torch.cuda.stream(cs_out):
+                cs_out.wait_event(back_done)
+                q_host[b].copy_(sess.q, non_blocking=True)
+                s_host[b].copy_(sess.s, non_blocking=True)
+                out_done = ev()
+                out_done.record(cs_out)
+        if t1 is not None:
+            cs_out.wait_event(out_done)
+            t1.record(cs_out)
+
+    pipeline(1)  # warm-up
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    pipeline(steps, t0, t1)
+    torch.cuda.synchronize()
+    del g_dev[1]
+    return t0.elapsed_time(t1)
 
 
 def _time_calls(fn, stream, reps: int = 3):

@@ -406,6 +406,10 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
     // Newton-Schulz unit table, grouped by shape class (section 4.1: matrices
     // with matching shapes are grouped for batched GEMMs)
     for (size_t k = 0; k < members.size(); ++k) {
+        if (members[k].size() > 65535) {  // a class's units span one grid dimension
+            delete p;
+            return HM_ERR_GEOMETRY;
+        }
         NsClassDev c{};
         const hm_unit_desc& u0 = units[members[k][0]];
         c.m = std::min(u0.rows, u0.cols);

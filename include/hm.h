@@ -149,8 +149,9 @@ typedef struct {
 typedef struct hm_muon_plan hm_muon_plan;
 
 /* Plans the update of the units (sorted, disjoint, tiling [0, n) exactly:
- * else HM_ERR_UNITS; rows*cols a multiple of 32 and cols <= 65535: else
- * HM_ERR_ALIGN / HM_ERR_GEOMETRY).  Classifies each unit as local (one z1
+ * else HM_ERR_UNITS; rows*cols a multiple of 32: else HM_ERR_ALIGN; rows and
+ * cols at most 2^20 and at most 65535 units per shape class: else
+ * HM_ERR_GEOMETRY).  Classifies each unit as local (one z1
  * fragment) or straddling, picks its execution rank (owner of its first
  * element), groups units by Newton-Schulz shape class (min, max of rows,
  * cols) and lays out the workspace.  Host only. */
@@ -213,7 +214,9 @@ typedef struct {  /* device roots, each in the chain's emulated layout */
 
 /* Runs the selected stages, in the order above, on `stream`.  u and v of
  * straddling units live in the workspace staging; v of local units is
- * written to the v root at the unit's own offsets. */
+ * written to the v root at the unit's own offsets.  A plan serves one stream
+ * at a time: calls on one plan must not run concurrently (they share the
+ * workspace and the plan's cached per-unit steps). */
 hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs* bufs,
                             const hm_muon_hparams* hp, void* workspace, size_t workspace_bytes,
                             int stages, void* stream);
