@@ -336,6 +336,7 @@ double alpha_of(int mode, int rows, int cols) {
 struct hm_muon_plan {
     hm_chain chain;
     std::vector<std::vector<int32_t>> sym_tab;  // per class: triangular tile list
+    std::vector<std::vector<int32_t>> pair_tab; // per class: the same for 256 x 256 tiles
     std::vector<hm_unit_desc> units;
     std::vector<UnitPlan> up;
     std::vector<NsClassDev> classes;
@@ -433,6 +434,15 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
                         if (tn * bn + bn - 1 >= tm * 128) tab.push_back((tm << 16) | tn);
             c.sym_tiles = static_cast<int32_t>(tab.size());
             p->sym_tab.push_back(tab);
+            // 256 x 256 tiles (CTA pairs): tn >= tm, bands of 4 tile-rows
+            std::vector<int32_t> tab2;
+            const int t2 = (c.mp + 255) / 256;
+            for (int g0 = 0; g0 < t2; g0 += 4)
+                for (int tn = 0; tn < t2; ++tn)
+                    for (int tm = g0; tm < std::min(t2, g0 + 4); ++tm)
+                        if (tn >= tm) tab2.push_back((tm << 16) | tn);
+            c.pair_tiles = static_cast<int32_t>(tab2.size());
+            p->pair_tab.push_back(tab2);
         }
         c.parts = static_cast<int32_t>((ne + c.part_len - 1) / c.part_len);
         for (int i : members[k]) {
@@ -538,6 +548,7 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
         c.part_off = take(static_cast<size_t>(c.n_units) * c.parts * 4);
         c.inv_off = take(static_cast<size_t>(c.n_units) * 4);
         c.sym_off = take(static_cast<size_t>(c.sym_tiles) * 4);
+        c.pair_off = take(static_cast<size_t>(c.pair_tiles) * 4);
     }
     p->ws_bytes = std::max<size_t>(off, kWsAlign);
     *out = p;
@@ -630,7 +641,8 @@ extern "C" hm_status muon_plan_upload(hm_muon_plan* p, void* workspace, size_t w
         put(p->off_nsu, p->ns_units.data(), p->ns_units.size() * sizeof(NsUnit)) != cudaSuccess)
         return HM_ERR_CUDA;
     for (size_t k = 0; k < p->classes.size(); ++k)
-        if (put(p->classes[k].sym_off, p->sym_tab[k].data(), p->sym_tab[k].size() * 4) != cudaSuccess)
+        if (put(p->classes[k].sym_off, p->sym_tab[k].data(), p->sym_tab[k].size() * 4) != cudaSuccess ||
+            put(p->classes[k].pair_off, p->pair_tab[k].data(), p->pair_tab[k].size() * 4) != cudaSuccess)
             return HM_ERR_CUDA;
     if (put(p->off_f0x, p->f0x_tab.data(), p->f0x_tab.size() * sizeof(Range)) != cudaSuccess) return HM_ERR_CUDA;
     p->maps.assign(p->classes.size(), ClassMaps{});
@@ -737,6 +749,7 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
         // HM_ERR_TIMEOUT in the device error word.
         const char* inj = std::getenv("HM_INJECT_NS_WAIT_TIMEOUT");
         bool inject = inj && inj[0] == '1';
+
         for (size_t k = 0; k < p->classes.size(); ++k) {
             const NsClassDev& c = p->classes[k];
             const ClassMaps& mp = p->maps[k];
@@ -757,7 +770,15 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g1.sym = 1;
                 g1.inject_no_ready = inject ? 1 : 0;
                 inject = false;
-                if (hm::launch_ns_gemm(mp.x_a[cur], mp.x_b[cur], g1, mp.bn1, 0, s) != cudaSuccess) return HM_ERR_CUDA;
+                // classes with at least 256 rows run on CTA pairs (256 x 256 tiles)
+                const bool pair = c.mp >= 256;
+                if (pair) {
+                    g1.tile_tab = reinterpret_cast<const int32_t*>(ws + c.pair_off);
+                    g1.tab_len = c.pair_tiles;
+                    if (hm::launch_ns_gemm_pair(mp.x_a[cur], mp.x_a[cur], g1, 0, s) != cudaSuccess) return HM_ERR_CUDA;
+                } else if (hm::launch_ns_gemm(mp.x_a[cur], mp.x_b[cur], g1, mp.bn1, 0, s) != cudaSuccess) {
+                    return HM_ERR_CUDA;
+                }
                 g1.inject_no_ready = 0;
 
                 hm::GemmParams g2 = g1;
@@ -765,7 +786,9 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g2.epi = hm::kEpiPoly; g2.alpha = hp->ns_c; g2.beta = hp->ns_b;
                 g2.add = bf(c.a_off); g2.add_us = g1.out_us; g2.ld_add = c.mp;
                 g2.out = bf(c.b_off);
-                if (hm::launch_ns_gemm(mp.a_a, mp.a_b, g2, mp.bn1, 0, s) != cudaSuccess) return HM_ERR_CUDA;
+                if (pair ? hm::launch_ns_gemm_pair(mp.a_a, mp.a_a, g2, 0, s) != cudaSuccess
+                         : hm::launch_ns_gemm(mp.a_a, mp.a_b, g2, mp.bn1, 0, s) != cudaSuccess)
+                    return HM_ERR_CUDA;
 
                 const bool last = it + 1 == hp->ns_steps;
                 hm::GemmParams g3{};
@@ -777,7 +800,12 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g3.m_real = c.m; g3.n_real = c.n;
                 g3.group_m = c.mp / 128;  // column bands: each X panel is fetched once per unit
                 g3.err = g1.err;
-                if (hm::launch_ns_gemm(mp.b_a, mp.x_mn[cur], g3, mp.bn3, 1, s) != cudaSuccess) return HM_ERR_CUDA;
+                if (pair) {
+                    g3.group_m = (c.mp + 255) / 256;
+                    if (hm::launch_ns_gemm_pair(mp.b_a, mp.x_mn[cur], g3, 1, s) != cudaSuccess) return HM_ERR_CUDA;
+                } else if (hm::launch_ns_gemm(mp.b_a, mp.x_mn[cur], g3, mp.bn3, 1, s) != cudaSuccess) {
+                    return HM_ERR_CUDA;
+                }
                 cur ^= 1;
             }
         }

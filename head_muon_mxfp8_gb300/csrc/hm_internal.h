@@ -68,6 +68,8 @@ struct NsClassDev {
     size_t x_off[2], a_off, b_off, part_off, inv_off;  // workspace bytes
     int32_t sym_tiles;   // tiles of the mp x mp output on or above the diagonal
     size_t sym_off;      // workspace bytes: their (tm << 16 | tn) list, L2-friendly order
+    int32_t pair_tiles;  // the same for the 256 x 256 tiles of the CTA-pair kernel
+    size_t pair_off;
 };
 
 // Epilogue kinds of the Newton-Schulz GEMM.
@@ -163,5 +165,9 @@ cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, cons
 // b_mn: the B operand is MN-major (its map has 64 x 64 boxes, N innermost)
 cudaError_t launch_ns_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p,
                            int bn, int b_mn, cudaStream_t st);
+// CTA-pair (cta_group::2) variant: 256 x 256 tiles, M a multiple of 128; both
+// operand maps use 128-row boxes (64 x 64 boxes for an MN-major B)
+cudaError_t launch_ns_gemm_pair(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p, int b_mn,
+                                cudaStream_t st);
 
 }  // namespace hm

@@ -322,10 +322,11 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& x, float* f) {
 }
 __device__ __forceinline__ uint32_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
+// i_base: first output row of this CTA's 128-row slab of the tile.
 template <int BN>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int tm, int tn, int row, uint32_t taddr,
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_base, int tn, int row, uint32_t taddr,
                                               float* stage, int half) {
-    const int i = tm * BM + row;
+    const int i = i_base + row;
 #pragma unroll 1
     for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
         const int j0 = tn * BN + c * 32;
@@ -529,7 +530,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            epilogue_tile<BN>(p, u, tm, tn, row,
+            epilogue_tile<BN>(p, u, tm * BM, tn, row,
                               tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN),
                               epi_stage + (warp - 2) * 32 * 33, half);
             tc_fence_before();
@@ -543,6 +544,267 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
+}
+
+// ---------------------------------------------------------------------------
+// CTA-pair variant (cta_group::2): a cluster of two CTAs computes one
+// 256 x 256 output tile.  Each CTA loads its own 128 rows of A and half of
+// B (128 rows K-major, or 128 columns MN-major) into its shared memory; the
+// even CTA of the pair issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
+// K = 16), which reads both CTAs' operands and writes rows 0-127 of D into
+// the even CTA's TMEM and rows 128-255 into the odd CTA's.  Per SM this halves
+// the B operand traffic of the 1-CTA 128 x 256 tile.  Barriers:
+//   full[s]   even CTA only: one expect_tx for both CTAs' bytes; both CTAs'
+//             TMA loads complete_tx on it (cta_group::2 TMA);
+//   empty[s]  in both CTAs, arrived by the MMA commit multicast to the pair;
+//   tfull[b]  in both CTAs, MMA commit multicast;
+//   tempty[b] even CTA only, arrived by the epilogue threads of both CTAs.
+// Every wait is bounded as in the 1-CTA kernel; a cluster barrier before the
+// end keeps each CTA's shared memory alive while its peer may still read it.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                                                 int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+
+template <bool B_MN>
+struct PairCfg {
+    static constexpr int BNP = 256;                 // N of the pair tile
+    static constexpr int STAGES = 6;
+    static constexpr int A_BYTES = BM * BK * 2;     // this CTA's 128 rows of A
+    static constexpr int B_BYTES = 128 * BK * 2;    // this CTA's half of B
+    static constexpr int TMEM_COLS = 2 * BNP;
+    static constexpr int EPI_BYTES = kEpiWarps * 32 * 33 * 4;
+    static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + EPI_BYTES + 1024 + 256;
+    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (B_MN ? (1u << 16) : 0u) |
+                                      (static_cast<uint32_t>(BNP >> 3) << 17) |
+                                      (static_cast<uint32_t>(256 >> 4) << 24);
+    static constexpr uint64_t B_KSTEP = B_MN ? (2048 >> 4) : (32 >> 4);
+};
+
+template <bool B_MN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
+                        const __grid_constant__ GemmParams p) {
+    using C = PairCfg<B_MN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sa = smem;
+    uint8_t* sb = sa + C::STAGES * C::A_BYTES;
+    float* epi_stage = reinterpret_cast<float*>(sb + C::STAGES * C::B_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sb + C::STAGES * C::B_BYTES + C::EPI_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* tfull = bars + 2 * C::STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* bail = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank() & 1u;
+    const bool leader = rank == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tfull[b]), 1);
+            mbar_init(smem_u32(&tempty[b]), 2 * 32 * kEpiWarps);
+        }
+        mbar_init(smem_u32(drain), 1);
+        *bail = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int per_unit = p.tile_tab ? p.tab_len : p.tiles_m * p.tiles_n;
+    const int total = p.units * per_unit;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, armed = 0, armed_par = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += npairs) {
+                int u, tm, tn;
+                decode_tile(t, p, u, tm, tn);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, p.err, bail)) { ok = false; break; }
+                    armed |= 1u << s;
+                    armed_par = (armed_par & ~(1u << s)) | (ph << s);
+                    const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+                    if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * (C::A_BYTES + C::B_BYTES));
+                    tma_load_3d_pair(smem_u32(sa + s * C::A_BYTES), &tma, fb, kb * BK, tm * 256 + rank * 128, u);
+                    if (B_MN) {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_3d_pair(smem_u32(sb + s * C::B_BYTES + c * 8192), &tmb, fb,
+                                             tn * C::BNP + rank * 128 + c * 64, kb * BK, u);
+                    } else {
+                        tma_load_3d_pair(smem_u32(sb + s * C::B_BYTES), &tmb, fb, kb * BK, tn * C::BNP + rank * 128, u);
+                    }
+                    if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+                }
+            }
+            // the even CTA's full barriers count both CTAs' bytes: waiting on
+            // them covers every copy of the pair still in flight
+            if (leader)
+                for (int k = 0; k < C::STAGES; ++k)
+                    if (armed & (1u << k)) mbar_wait(smem_u32(&full[k]), (armed_par >> k) & 1u, p.err, bail, false);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            int s = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += npairs) {
+                if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1u, p.err, bail)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * C::BNP);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&full[s]), ph, p.err, bail)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t ad = desc_sw128(smem_u32(sa + s * C::A_BYTES));
+                    const uint32_t bs = smem_u32(sb + s * C::B_BYTES);
+                    const uint64_t bd = B_MN ? desc_mn_sw128(bs) : desc_sw128(bs);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16_pair(d, ad + 2 * kk, bd + C::B_KSTEP * kk, C::IDESC, (kb | kk) != 0);
+                    umma_commit_pair(smem_u32(&empty[s]));
+                    if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                if (!p.inject_no_ready) umma_commit_pair(smem_u32(&tfull[acc]));
+                acc ^= 1;
+                if (!acc) aph ^= 1u;
+            }
+            umma_commit_pair(smem_u32(drain));
+            mbar_wait(smem_u32(drain), 0, p.err, bail, false);
+        }
+    } else {
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int row = q * 32 + lane;
+        const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
+        const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int t = pair; t < total; t += npairs) {
+            int u, tm, tn;
+            decode_tile(t, p, u, tm, tn);
+            bool ok = mbar_wait(smem_u32(&tfull[acc]), aph, p.err, bail);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const int i_base = tm * 256 + static_cast<int>(rank) * 128;
+            if (i_base < p.M)  // a slab beyond the last row (M a multiple of 128) holds no output
+                epilogue_tile<C::BNP>(p, u, i_base, tn, row,
+                                      tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::BNP),
+                                      epi_stage + (warp - 2) * 32 * 33, half);
+            tc_fence_before();
+            mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+            acc ^= 1;
+            if (!acc) aph ^= 1u;
+        }
+    }
+    // the peer's MMAs read this CTA's shared memory and write its TMEM: keep
+    // both alive until every role of both CTAs is done
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    }
+}
+
+template <bool B_MN>
+cudaError_t launch_gemm_pair(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p0, cudaStream_t st) {
+    using C = PairCfg<B_MN>;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel<B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    GemmParams p = p0;
+    p.tiles_m = (p.M + 255) / 256;
+    p.tiles_n = (p.N + C::BNP - 1) / C::BNP;
+    p.num_kb = (p.K + BK - 1) / BK;
+    const int total = p.units * (p.tile_tab ? p.tab_len : p.tiles_m * p.tiles_n);
+    if (total == 0) return cudaSuccess;
+    const int pairs = total < device_sm_count() / 2 ? total : device_sm_count() / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<B_MN>, tma, tmb, p);
 }
 
 template <int BN, bool B_MN>
@@ -587,6 +849,11 @@ cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, cons
     ns_prepare_kernel<<<g, 256, 0, st>>>(units_dev, u_root, u_stage, reinterpret_cast<const float*>(ws + c.inv_off),
                                          reinterpret_cast<uint16_t*>(ws + c.x_off[0]), c.m, c.n, c.np);
     return cudaGetLastError();
+}
+
+cudaError_t launch_ns_gemm_pair(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p, int b_mn,
+                                cudaStream_t st) {
+    return b_mn ? launch_gemm_pair<true>(tma, tmb, p, st) : launch_gemm_pair<false>(tma, tmb, p, st);
 }
 
 cudaError_t launch_ns_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p, int bn, int b_mn,

@@ -24,9 +24,15 @@ def dev(hm):
     return torch.device("cuda:0")
 
 
-def test_injected_wait_timeout_is_reported_and_recovered(hm, dev):
+@pytest.mark.parametrize("name", ["tiny", "pair"])
+def test_injected_wait_timeout_is_reported_and_recovered(hm, dev, name):
+    """tiny: the first GEMM is a single-CTA launch (128-row class); pair: a
+    512 x 768 class, whose GEMMs run on CTA pairs (cta_group::2)."""
     from head_muon_mxfp8_gb300.session import MuonSession, muon_hparams
-    cfg = workloads.get("tiny")
+    if name == "pair":
+        cfg = workloads.scaled_muon("pair", [(512, 768, None), (768, 512, None)], so=4, sw=2, sg=2)
+    else:
+        cfg = workloads.get("tiny")
     data = workloads.generate(cfg, seed=41)
     s = MuonSession.from_config(cfg, device=dev)
     s.load("w", data["w"])
