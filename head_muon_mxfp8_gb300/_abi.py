@@ -97,6 +97,7 @@ _I32P = C.POINTER(C.c_int32)
 _SIGS = {
     "hm_status_str": (C.c_char_p, [C.c_int]),
     "hm_device_error": (C.c_int, [_I32P]),
+    "hm_kernel_launches": (C.c_int, [C.POINTER(C.c_int64)]),
     "create_data_tree": (C.c_int, [C.POINTER(_P), _P, C.c_size_t]),
     "data_tree_add_view": (C.c_int, [_P, C.c_int, C.c_size_t, C.c_int, C.c_int, _I64P, _I32P]),
     "data_tree_resolve": (C.c_int, [_P, C.c_int, C.POINTER(_P), C.POINTER(C.c_size_t)]),
@@ -165,6 +166,13 @@ def _i64(vals):
 
 
 # ---- thin wrappers: same names as the C ABI --------------------------------
+def hm_kernel_launches() -> int:
+    """Kernels this thread has launched through the library so far."""
+    n = C.c_int64(0)
+    check("hm_kernel_launches", lib().hm_kernel_launches(C.byref(n)))
+    return n.value
+
+
 def hm_device_error() -> int:
     code = C.c_int32(0)
     check("hm_device_error", lib().hm_device_error(C.byref(code)))

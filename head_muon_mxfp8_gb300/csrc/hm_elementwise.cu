@@ -388,6 +388,12 @@ __global__ void __launch_bounds__(kThreads) adamw_kernel(float* __restrict__ w, 
 }  // namespace
 
 // ---------------------------------------------------------------------------
+namespace {
+thread_local int64_t t_launches = 0;
+}
+void note_launch() { ++t_launches; }
+int64_t launches_issued() { return t_launches; }
+
 int device_sm_count() {
     static int cached[64] = {0};
     int dev = 0;
@@ -415,12 +421,14 @@ int32_t* device_error_word() {
 cudaError_t launch_f0(const RangeArgs& ra, float* m, const float* g, uint16_t* u, uint16_t* u_stage, float mu,
                       int nesterov, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
+    note_launch();
     f0_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, m, g, u, u_stage, mu, nesterov);
     return cudaGetLastError();
 }
 
 cudaError_t launch_copy_bf16(const RangeArgs& ra, const uint16_t* src, uint16_t* dst, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
+    note_launch();
     copy_bf16_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, src, dst);
     return cudaGetLastError();
 }
@@ -428,12 +436,14 @@ cudaError_t launch_copy_bf16(const RangeArgs& ra, const uint16_t* src, uint16_t*
 cudaError_t launch_f2(const RangeArgs& ra, float* w, const float* v_root, const float* v_stage, float decay,
                       int has_decay, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
+    note_launch();
     f2_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, w, v_root, v_stage, decay, has_decay);
     return cudaGetLastError();
 }
 
 cudaError_t launch_requant(const RangeArgs& ra, const float* w, uint8_t* q, uint8_t* s, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
+    note_launch();
     requant_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, w, q, s);
     return cudaGetLastError();
 }
@@ -441,12 +451,14 @@ cudaError_t launch_requant(const RangeArgs& ra, const float* w, uint8_t* q, uint
 cudaError_t launch_f2_requant(const RangeArgs& ra, float* w, const float* v_root, const float* v_stage, uint8_t* q,
                               uint8_t* s, float decay, int has_decay, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
+    note_launch();
     f2_requant_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, w, v_root, v_stage, q, s, decay, has_decay);
     return cudaGetLastError();
 }
 
 cudaError_t launch_reduce_scatter(const RangeArgs& ra, const RsArgs& a, float* g, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
+    note_launch();
     reduce_scatter_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, a, g);
     return cudaGetLastError();
 }
@@ -461,6 +473,7 @@ cudaError_t launch_adamw(float* w, const void* g, int g_bf16, float* m, float* v
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
+    note_launch();
     if (g_bf16)
         adamw_kernel<true><<<static_cast<int>(blocks), kThreads, 0, st>>>(w, g, m, v, n, a);
     else

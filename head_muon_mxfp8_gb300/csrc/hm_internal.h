@@ -97,6 +97,7 @@ struct GemmParams {
     int32_t sym;              // symmetric output: write (i, j) and (j, i) for j >= i only
     int32_t group_m;          // tile-rows per raster band of the full grid (0 = 8)
     int32_t inject_no_ready;  // failure test: never signal an accumulator as ready
+    int32_t unit0;            // index of the first unit this launch covers
 };
 
 // chain geometry the device needs: z1 edges and the segment base of every chunk
@@ -131,6 +132,10 @@ struct RelayoutArgs {
 };
 
 // ---- launchers (return cudaGetLastError() of the launch) -----------------
+// Kernels launched by the calling thread through the library (every launch
+// site calls note_launch once per kernel it enqueues).
+void note_launch();
+int64_t launches_issued();
 int device_sm_count();
 int32_t* device_error_word();
 

@@ -142,6 +142,7 @@ cudaError_t launch_requant_32x32(const ChainArgs& ch, const Mx32Args& ta, const 
     int64_t blocks = (total + 3) / 4;
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
     if (blocks > cap) blocks = cap;
+    note_launch();
     requant_32x32_kernel<<<static_cast<int>(blocks), 128, 0, st>>>(ch, ta, w, q, scales);
     return cudaGetLastError();
 }
@@ -153,6 +154,7 @@ cudaError_t launch_scale_relayout(const RelayoutArgs& ra, const uint8_t* src, ui
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
+    note_launch();
     scale_relayout_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(ra, src, dst);
     return cudaGetLastError();
 }

@@ -146,6 +146,7 @@ extern "C" hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int3
     ok = ok && map_bf16(&b_map, ws + c.b_off, c.mp, c.mp, 128);
     if (!ok) return HM_ERR_CUDA;
 
+    hm::note_launch();
     write_unit_kernel<<<1, 1, 0, st>>>(unit_dev, unit);
     if (cudaGetLastError() != cudaSuccess) return HM_ERR_CUDA;
     if (hm::launch_ns_norm(c, unit_dev, u, nullptr, ws, hp->eps, st) != cudaSuccess ||

@@ -297,6 +297,7 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, int& u, 
         const int32_t e = __ldg(p.tile_tab + (t - u * p.tab_len));
         tm = e >> 16;
         tn = e & 0xFFFF;
+        u += p.unit0;
         return;
     }
     const int per = p.tiles_m * p.tiles_n;
@@ -310,6 +311,7 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, int& u, 
     const int rr = r - g * group;
     tm = first + rr % gm;
     tn = rr / gm;
+    u += p.unit0;
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& x, float* f) {
@@ -804,6 +806,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tma, const CUtensorMap& tmb, con
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    note_launch();
     return cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<B_MN>, tma, tmb, p);
 }
 
@@ -825,6 +828,7 @@ cudaError_t launch_gemm_bn(const CUtensorMap& tma, const CUtensorMap& tmb, const
     const int total = p.units * (p.tile_tab ? p.tab_len : p.tiles_m * p.tiles_n);
     if (total == 0) return cudaSuccess;
     const int grid = total < device_sm_count() ? total : device_sm_count();
+    note_launch();
     ns_gemm_kernel<BN, B_MN><<<grid, kGemmThreads, C::SMEM, st>>>(tma, tmb, p);
     return cudaGetLastError();
 }
@@ -836,9 +840,11 @@ cudaError_t launch_ns_norm(const NsClassDev& c, const NsUnit* units_dev, const u
     float* partials = reinterpret_cast<float*>(ws + c.part_off);
     float* inv = reinterpret_cast<float*>(ws + c.inv_off);
     dim3 g1(c.parts, c.n_units);
+    note_launch();
     ns_norm_partial_kernel<<<g1, 256, 0, st>>>(units_dev, u_root, u_stage, partials, c.parts, c.part_len);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    note_launch();
     ns_norm_final_kernel<<<(c.n_units + 7) / 8, 256, 0, st>>>(partials, c.parts, inv, eps, c.n_units);
     return cudaGetLastError();
 }
@@ -846,6 +852,7 @@ cudaError_t launch_ns_norm(const NsClassDev& c, const NsUnit* units_dev, const u
 cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
                               const uint16_t* u_stage, char* ws, cudaStream_t st) {
     dim3 g(c.np / 64, c.mp / 64, c.n_units);
+    note_launch();
     ns_prepare_kernel<<<g, 256, 0, st>>>(units_dev, u_root, u_stage, reinterpret_cast<const float*>(ws + c.inv_off),
                                          reinterpret_cast<uint16_t*>(ws + c.x_off[0]), c.m, c.n, c.np);
     return cudaGetLastError();

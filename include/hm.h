@@ -69,6 +69,14 @@ const char* hm_status_str(hm_status s);
  * device-side wait that gave up, HM_ERR_TIMEOUT).  Synchronises the device. */
 hm_status hm_device_error(int* code);
 
+/* Number of kernels the calling thread has enqueued through this library
+ * since it loaded (every entry point counts each kernel it launches, on any
+ * stream).  Host-only: reads a thread-local counter, touches no device.  The
+ * difference of two readings around a sequence of calls is the number of
+ * kernel launches that sequence made.  The pages define no such call; it
+ * exists so that a caller can report how many kernels a step runs. */
+hm_status hm_kernel_launches(int64_t* count);
+
 /* ------------------------------------------------------------------------ */
 /* Data tree (section 3.2 "Data Tree"): a root node owns one allocation; every
  * other node is a view (parent, byte offset, dtype, shape) and reaches the

@@ -206,3 +206,12 @@ def test_checks_that_precede_any_launch(hm):
     assert L.mxfp8_requant_packed(C.c_void_p(256), C.c_void_p(256), C.c_void_p(256), arr, 1, None) == \
         hm.HM_ERR_ALIGN
     assert L.mxfp8_requant_packed(None, None, None, None, 0, None) == hm.HM_OK
+
+
+def test_kernel_launch_counter_is_host_only(hm):
+    """The launch counter reads without a device, and a call rejected by its
+    host-side checks launches nothing."""
+    n0 = hm.hm_kernel_launches()
+    assert n0 >= 0
+    assert hm.lib().adamw_update_flat(None, None, hm.HM_BF16, None, None, 16, None, None) == hm.HM_ERR_ARG
+    assert hm.hm_kernel_launches() == n0

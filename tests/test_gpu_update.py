@@ -295,3 +295,22 @@ def test_empty_inputs_are_noops(hm, dev):
     hm.mxfp8_requant_packed(x.data_ptr(), x.data_ptr(), x.data_ptr(), [(0, 0, 0, 0, 32)])
     torch.cuda.synchronize()
     assert hm.hm_device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixed"])
+def test_kernel_launch_count_of_one_fused_update(hm, dev, name):
+    """One fused update launches f0 (with the gather), per shape class the
+    norm partials, the norm total, the prepare pass and 3 products per
+    Newton-Schulz iteration, then f2 with the requant: the library's launch
+    counter reports exactly that many kernels."""
+    cfg = workloads.get(name)
+    data = workloads.generate(cfg, seed=5)
+    s = _session(cfg, dev)
+    s.load("w", data["w"])
+    s.load("g", data["g"])
+    hp = _hp(cfg.muon)
+    before = hm.hm_kernel_launches()
+    s.run(hp, hm.HM_STAGE_ALL_FUSED)
+    n = hm.hm_kernel_launches() - before
+    torch.cuda.synchronize()
+    assert n == 2 + s.info.n_classes * (3 + 3 * cfg.muon.ns_steps)
