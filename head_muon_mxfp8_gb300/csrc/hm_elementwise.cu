@@ -41,11 +41,7 @@ __device__ __forceinline__ int find_range(const RangeArgs& ra, int64_t v) {
     return lo;
 }
 
-int grid_for(int64_t total) {
-    const int64_t tiles = (total + kTile - 1) / kTile;
-    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
-    return static_cast<int>(tiles < cap ? tiles : cap);
-}
+int64_t tiles_of(int64_t total) { return (total + kTile - 1) / kTile; }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
@@ -422,14 +418,16 @@ cudaError_t launch_f0(const RangeArgs& ra, float* m, const float* g, uint16_t* u
                       int nesterov, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
     note_launch();
-    f0_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, m, g, u, u_stage, mu, nesterov);
+    const int grid = resident_grid(f0_kernel, kThreads, tiles_of(ra.total));
+    f0_kernel<<<grid, kThreads, 0, st>>>(ra, m, g, u, u_stage, mu, nesterov);
     return cudaGetLastError();
 }
 
 cudaError_t launch_copy_bf16(const RangeArgs& ra, const uint16_t* src, uint16_t* dst, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
     note_launch();
-    copy_bf16_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, src, dst);
+    const int grid = resident_grid(copy_bf16_kernel, kThreads, tiles_of(ra.total));
+    copy_bf16_kernel<<<grid, kThreads, 0, st>>>(ra, src, dst);
     return cudaGetLastError();
 }
 
@@ -437,14 +435,16 @@ cudaError_t launch_f2(const RangeArgs& ra, float* w, const float* v_root, const 
                       int has_decay, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
     note_launch();
-    f2_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, w, v_root, v_stage, decay, has_decay);
+    const int grid = resident_grid(f2_kernel, kThreads, tiles_of(ra.total));
+    f2_kernel<<<grid, kThreads, 0, st>>>(ra, w, v_root, v_stage, decay, has_decay);
     return cudaGetLastError();
 }
 
 cudaError_t launch_requant(const RangeArgs& ra, const float* w, uint8_t* q, uint8_t* s, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
     note_launch();
-    requant_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, w, q, s);
+    const int grid = resident_grid(requant_kernel, kThreads, tiles_of(ra.total));
+    requant_kernel<<<grid, kThreads, 0, st>>>(ra, w, q, s);
     return cudaGetLastError();
 }
 
@@ -452,14 +452,16 @@ cudaError_t launch_f2_requant(const RangeArgs& ra, float* w, const float* v_root
                               uint8_t* s, float decay, int has_decay, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
     note_launch();
-    f2_requant_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, w, v_root, v_stage, q, s, decay, has_decay);
+    const int grid = resident_grid(f2_requant_kernel, kThreads, tiles_of(ra.total));
+    f2_requant_kernel<<<grid, kThreads, 0, st>>>(ra, w, v_root, v_stage, q, s, decay, has_decay);
     return cudaGetLastError();
 }
 
 cudaError_t launch_reduce_scatter(const RangeArgs& ra, const RsArgs& a, float* g, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
     note_launch();
-    reduce_scatter_kernel<<<grid_for(ra.total), kThreads, 0, st>>>(ra, a, g);
+    const int grid = resident_grid(reduce_scatter_kernel, kThreads, tiles_of(ra.total));
+    reduce_scatter_kernel<<<grid, kThreads, 0, st>>>(ra, a, g);
     return cudaGetLastError();
 }
 
@@ -469,15 +471,15 @@ cudaError_t launch_adamw(float* w, const void* g, int g_bf16, float* m, float* v
     if (n == 0) return cudaSuccess;
     AdamArgs a{beta1, beta2, eps, decay, step_size, inv_sqrt_bc2};
     const int64_t nv = n / 4;
-    int64_t blocks = (nv + kThreads - 1) / kThreads;
-    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
+    const int64_t blocks = (nv + kThreads - 1) / kThreads;
     note_launch();
-    if (g_bf16)
-        adamw_kernel<true><<<static_cast<int>(blocks), kThreads, 0, st>>>(w, g, m, v, n, a);
-    else
-        adamw_kernel<false><<<static_cast<int>(blocks), kThreads, 0, st>>>(w, g, m, v, n, a);
+    if (g_bf16) {
+        const int grid = resident_grid(adamw_kernel<true>, kThreads, blocks);
+        adamw_kernel<true><<<grid, kThreads, 0, st>>>(w, g, m, v, n, a);
+    } else {
+        const int grid = resident_grid(adamw_kernel<false>, kThreads, blocks);
+        adamw_kernel<false><<<grid, kThreads, 0, st>>>(w, g, m, v, n, a);
+    }
     return cudaGetLastError();
 }
 

@@ -137,6 +137,20 @@ struct RelayoutArgs {
 void note_launch();
 int64_t launches_issued();
 int device_sm_count();
+
+// Grid of a grid-stride kernel: every CTA resident at once (SM count x the
+// CTAs per SM that the kernel's registers, shared memory and block size
+// allow), or one CTA per work item when there are fewer.  A larger grid
+// would leave its last CTAs to run alone after the others have finished.
+template <class Kernel>
+inline int resident_grid(Kernel kernel, int threads, int64_t items) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * per_sm;
+    if (items < 1) items = 1;
+    return static_cast<int>(items < cap ? items : cap);
+}
 int32_t* device_error_word();
 
 cudaError_t launch_f0(const RangeArgs& ra, float* m, const float* g, uint16_t* u, uint16_t* u_stage,

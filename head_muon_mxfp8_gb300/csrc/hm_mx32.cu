@@ -139,23 +139,18 @@ cudaError_t launch_requant_32x32(const ChainArgs& ch, const Mx32Args& ta, const 
                                  uint8_t* scales, cudaStream_t st) {
     const int64_t total = ta.block_prefix[ta.n];
     if (total == 0) return cudaSuccess;
-    int64_t blocks = (total + 3) / 4;
-    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
-    if (blocks > cap) blocks = cap;
+    const int64_t blocks = (total + 3) / 4;
     note_launch();
-    requant_32x32_kernel<<<static_cast<int>(blocks), 128, 0, st>>>(ch, ta, w, q, scales);
+    requant_32x32_kernel<<<resident_grid(requant_32x32_kernel, 128, blocks), 128, 0, st>>>(ch, ta, w, q, scales);
     return cudaGetLastError();
 }
 
 cudaError_t launch_scale_relayout(const RelayoutArgs& ra, const uint8_t* src, uint8_t* dst, cudaStream_t st) {
     const int64_t total = ra.out_prefix[ra.n];
     if (total == 0) return cudaSuccess;
-    int64_t blocks = (total / 16 + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
+    const int64_t blocks = (total / 16 + 255) / 256;
     note_launch();
-    scale_relayout_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(ra, src, dst);
+    scale_relayout_kernel<<<resident_grid(scale_relayout_kernel, 256, blocks), 256, 0, st>>>(ra, src, dst);
     return cudaGetLastError();
 }
 

@@ -19,7 +19,9 @@
 // contracts rows of B with columns of X: B is K-major, X is read as an
 // MN-major operand (N contiguous), so X^T is never stored.
 //
-// GEMM kernel: persistent, one CTA per SM, 192 threads:
+// GEMM kernels: persistent, 320 threads per CTA.  ns_gemm_kernel runs one
+// CTA per SM on 128-row tiles; ns_gemm_pair_kernel (further down) runs CTA
+// pairs on 256 x 256 tiles with the same roles.  Single CTA:
 //   warp 0      TMA producer: a 128x64 A box and a BNx64 K-major B box (or
 //               BN/64 boxes of 64 N x 64 K for an MN-major B), 128-byte
 //               swizzle, STAGES-deep mbarrier ring;
@@ -324,14 +326,43 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& x, float* f) {
 }
 __device__ __forceinline__ uint32_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
-// i_base: first output row of this CTA's 128-row slab of the tile.
+// Epilogues that add aX read the addend with 4 lanes per row (see below).
+__device__ __forceinline__ bool addend_coalesced(const GemmParams& p) {
+    return (p.epi == kEpiUpdate || p.epi == kEpiFinal) && !p.sym;
+}
+
+// With a short K (B X of the 128-row head class: two k-blocks) the epilogue,
+// not the MMA, sets the pace, so the first addend chunk of a tile is loaded
+// before its accumulator is ready.  With a long K the addend is left until
+// the accumulator is ready: by then the tile's TMA loads have brought those
+// rows of X into the L2, and an early read would fetch them from DRAM.
+constexpr int kEarlyAddendKb = 8;
+
+// Loads one 32 x 32 chunk of the addend X (rows i0.., columns j0..) in the
+// coalesced pattern: lane l holds row i0 + l/4 + 8s, columns j0 + 8(l%4)..+7.
+__device__ __forceinline__ void load_addend_chunk(const GemmParams& p, int u, int i0, int j0, uint4 (&a)[4]) {
+    const int lane = threadIdx.x & 31;
+    if (j0 >= p.N) return;
+    const uint16_t* ab = p.add + u * p.add_us + j0 + (lane & 3) * 8;
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+        a[s] = __ldg(reinterpret_cast<const uint4*>(ab + static_cast<int64_t>(i0 + (lane >> 2) + 8 * s) * p.ld_add));
+}
+
+// i_base: first output row of this CTA's 128-row slab of the tile.  `next`
+// holds the addend of the warp's first chunk when addend_coalesced(p): the
+// caller loads it before waiting for the accumulator, and each chunk loads
+// the next one's before it works on its own.
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_base, int tn, int row, uint32_t taddr,
-                                              float* stage, int half) {
+                                              float* stage, int half, uint4 (&next)[4]) {
     const int i = i_base + row;
+    const int c_end = (half + 1) * (BN / 64);
 #pragma unroll 1
-    for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
+    for (int c = half * (BN / 64); c < c_end; ++c) {
         const int j0 = tn * BN + c * 32;
+        uint4 a[4] = {next[0], next[1], next[2], next[3]};
+        if (addend_coalesced(p) && c + 1 < c_end) load_addend_chunk(p, u, i - (threadIdx.x & 31), j0 + 32, next);
         uint32_t r[32];
         __syncwarp();
         tmem_ld32(taddr + c * 32, r);
@@ -342,7 +373,61 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
         float v[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * p.alpha;
-        if (p.epi != kEpiGram) {
+        if ((p.epi == kEpiUpdate || p.epi == kEpiFinal) && !p.sym) {
+            // aX + BX through the warp's staging: the lane that holds row i parks
+            // its 32 sums, then every load of the addend (and every store of X')
+            // covers 8 rows x 64 contiguous bytes, 4 lanes per row, instead of
+            // 32 rows x 16 bytes
+            const int lane = threadIdx.x & 31;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) stage[lane * 33 + k] = v[k];
+            __syncwarp();
+            const int cq = (lane & 3) * 8;
+            if (p.epi == kEpiUpdate) {
+                uint16_t* ob = p.out + u * p.out_us + j0 + cq;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const int rr = (lane >> 2) + 8 * s;
+                    float a8[8], o[8];
+                    unpack_bf16x8(a[s], a8);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) o[t] = fmaf(p.beta, a8[t], stage[rr * 33 + cq + t]);
+                    *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(i0 + rr) * p.ld_out) = make_uint4(
+                        bf16_bits(o[0]) | (bf16_bits(o[1]) << 16), bf16_bits(o[2]) | (bf16_bits(o[3]) << 16),
+                        bf16_bits(o[4]) | (bf16_bits(o[5]) << 16), bf16_bits(o[6]) | (bf16_bits(o[7]) << 16));
+                }
+                continue;
+            }
+            // last iteration: v = fp32(aX + BX) into the unit's own v location
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int rr = (lane >> 2) + 8 * s;
+                float a8[8];
+                unpack_bf16x8(a[s], a8);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) stage[rr * 33 + cq + t] = fmaf(p.beta, a8[t], stage[rr * 33 + cq + t]);
+            }
+            __syncwarp();
+            const NsUnit nu = p.ns_units[u];
+            float* dst = ((nu.flags & kNsVStaged) ? p.v_stage : p.v_root) + nu.v_off;
+            if (nu.flags & kNsTransposed) {
+                // v is X^T: for each k the 32 lanes write 32 consecutive floats
+                // of v's row j0 + k
+                if (i < p.m_real) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        if (j0 + k < p.n_real) dst[static_cast<int64_t>(j0 + k) * p.m_real + i] = stage[lane * 33 + k];
+                }
+            } else if (j0 + lane < p.n_real) {
+                // row-major v: each store instruction writes 128 contiguous bytes of one row
+#pragma unroll 4
+                for (int r2 = 0; r2 < 32; ++r2)
+                    if (i0 + r2 < p.m_real) dst[static_cast<int64_t>(i0 + r2) * p.n_real + j0 + lane] = stage[r2 * 33 + lane];
+            }
+            __syncwarp();
+            continue;
+        }
+        if (p.epi == kEpiPoly) {
             const uint4* ap = reinterpret_cast<const uint4*>(p.add + u * p.add_us + static_cast<int64_t>(i) * p.ld_add + j0);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -351,33 +436,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
 #pragma unroll
                 for (int k = 0; k < 8; ++k) v[q * 8 + k] = fmaf(p.beta, a8[k], v[q * 8 + k]);
             }
-        }
-        if (p.epi == kEpiFinal) {
-            const NsUnit nu = p.ns_units[u];
-            if (i < p.m_real && (nu.flags & kNsTransposed)) {
-                float* dst = ((nu.flags & kNsVStaged) ? p.v_stage : p.v_root) + nu.v_off;
-                {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        if (j0 + k < p.n_real) dst[static_cast<int64_t>(j0 + k) * p.m_real + i] = v[k];
-                }
-            }
-            if (!(nu.flags & kNsTransposed)) {
-                // row-major v: transpose the warp's 32 x 32 block through shared
-                // memory so that each store instruction writes 128 contiguous bytes
-                const int lane = threadIdx.x & 31;
-#pragma unroll
-                for (int k = 0; k < 32; ++k) stage[lane * 33 + k] = v[k];
-                __syncwarp();
-                float* dst = ((nu.flags & kNsVStaged) ? p.v_stage : p.v_root) + nu.v_off;
-                if (j0 + lane < p.n_real) {
-#pragma unroll 4
-                    for (int r2 = 0; r2 < 32; ++r2)
-                        if (i0 + r2 < p.m_real) dst[static_cast<int64_t>(i0 + r2) * p.n_real + j0 + lane] = stage[r2 * 33 + lane];
-                }
-                __syncwarp();
-            }
-            continue;
         }
         if (p.sym) {
             // symmetric output: this warp owns rows i0..i0+31; only elements
@@ -528,13 +586,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             int u, tm, tn;
             decode_tile(t, p, u, tm, tn);
+            uint4 first[4] = {};
+            const bool early = addend_coalesced(p) && p.num_kb <= kEarlyAddendKb;
+            if (early) load_addend_chunk(p, u, tm * BM + q * 32, tn * BN + half * (BN / 2), first);
             bool ok = mbar_wait(smem_u32(&tfull[acc]), aph, p.err, bail);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
+            if (addend_coalesced(p) && !early)
+                load_addend_chunk(p, u, tm * BM + q * 32, tn * BN + half * (BN / 2), first);
             epilogue_tile<BN>(p, u, tm * BM, tn, row,
                               tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN),
-                              epi_stage + (warp - 2) * 32 * 33, half);
+                              epi_stage + (warp - 2) * 32 * 33, half, first);
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[acc]));
             acc ^= 1;
@@ -749,15 +812,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int t = pair; t < total; t += npairs) {
             int u, tm, tn;
             decode_tile(t, p, u, tm, tn);
+            const int i_base = tm * 256 + static_cast<int>(rank) * 128;
+            uint4 first[4] = {};
+            const bool coalesced = addend_coalesced(p) && i_base < p.M;
+            const bool early = coalesced && p.num_kb <= kEarlyAddendKb;
+            if (early) load_addend_chunk(p, u, i_base + q * 32, tn * C::BNP + half * (C::BNP / 2), first);
             bool ok = mbar_wait(smem_u32(&tfull[acc]), aph, p.err, bail);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const int i_base = tm * 256 + static_cast<int>(rank) * 128;
+            if (coalesced && !early) load_addend_chunk(p, u, i_base + q * 32, tn * C::BNP + half * (C::BNP / 2), first);
             if (i_base < p.M)  // a slab beyond the last row (M a multiple of 128) holds no output
                 epilogue_tile<C::BNP>(p, u, i_base, tn, row,
                                       tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::BNP),
-                                      epi_stage + (warp - 2) * 32 * 33, half);
+                                      epi_stage + (warp - 2) * 32 * 33, half, first);
             tc_fence_before();
             mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
             acc ^= 1;
