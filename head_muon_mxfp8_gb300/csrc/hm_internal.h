@@ -129,7 +129,10 @@ struct RelayoutArgs {
     int64_t rows[kMaxRelayoutItems];
     int64_t kb[kMaxRelayoutItems];
     int32_t block_rows[kMaxRelayoutItems];
+    int32_t flags[kMaxRelayoutItems];  // kRelayout* bits
 };
+constexpr int kRelayoutSrcWords = 1;  // src + src offset and kb are multiples of 4: 4-byte loads
+constexpr int kRelayoutDst16 = 2;     // dst + dst offset is 16-byte aligned: one 16-byte store per group
 
 // ---- launchers (return cudaGetLastError() of the launch) -----------------
 // Kernels launched by the calling thread through the library (every launch

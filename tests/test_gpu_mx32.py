@@ -70,26 +70,33 @@ def test_requant_32x32_flat(hm, dev):
 
 
 def test_scale_relayout_128x4(hm, dev):
+    """Aligned items take 4-byte source loads and 16-byte stores; the others
+    (kb not a multiple of 4, a source or destination offset off alignment)
+    take byte accesses: both must give the oracle's layout."""
     rng = np.random.default_rng(25)
-    mats = [(256, 8, 1), (200, 5, 1), (64, 6, 32), (1408, 64, 32)]
+    # rows, kb, block_rows, source pad before the item, destination gap after it
+    mats = [(256, 8, 1, 0, 64), (200, 5, 1, 0, 67), (64, 6, 32, 0, 64), (1408, 64, 32, 0, 61),
+            (128, 12, 1, 1, 64), (384, 16, 1, 3, 64)]
     src_parts, items, refs = [], [], []
     s_off, d_off = 0, 0
-    for rows, kb, br in mats:
+    for rows, kb, br, s_pad, gap in mats:
         sf = rng.integers(0, 255, size=(rows // br, kb)).astype(np.uint8)
+        src_parts.append(np.full(s_pad, 0x77, dtype=np.uint8))
+        s_off += s_pad
         src_parts.append(sf.ravel())
         ref = OX.scale_tile_128x4(OX.expand_block_rows(sf, br) if br > 1 else sf)
         items.append((s_off, d_off, rows, kb, br))
         refs.append((d_off, ref))
         s_off += sf.size
-        d_off += ref.size + 64                                  # a gap between outputs
+        d_off += ref.size + gap                                 # a gap between outputs
     src = torch.from_numpy(np.concatenate(src_parts)).to(dev)
     dst = torch.full((d_off,), 0xEE, dtype=torch.uint8, device=dev)
     hm.mxfp8_scale_relayout(src.data_ptr(), dst.data_ptr(), items)
     torch.cuda.synchronize()
     out = dst.cpu().numpy()
-    for off, ref in refs:
+    for (off, ref), m in zip(refs, mats):
         assert np.array_equal(out[off:off + ref.size], ref)
-        assert (out[off + ref.size:off + ref.size + 64] == 0xEE).all()
+        assert (out[off + ref.size:off + ref.size + m[4]] == 0xEE).all()
 
 
 def test_requant_32x32_fullsize_lm_sampled(hm, dev):
