@@ -357,7 +357,7 @@ def run_ours(args, cfg):
 
     # ---- end to end: host gradient in, host MXFP8 runtime weight out -----
     e2e_steps = max(2, min(4, args.steps))
-    e2e_ms = e2e_pipelined(sess, hp, stream, e2e_steps, dist)
+    e2e_ms, copy_rates = e2e_pipelined(sess, hp, stream, e2e_steps, dist)
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     e2e_value = whole_job_rate(world, cfg.numel, e2e_steps, e2e_ms)
     h2d = sess.total * 4
@@ -432,6 +432,7 @@ def run_ours(args, cfg):
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+                        "copy_rates_gbs": copy_rates,
                         "note": "host gradient in, host MXFP8 weights + scales out, every step; copies on their own "
                                 "streams overlap the previous / next step's Newton-Schulz stage"},
                 "gpu_launches": launches, "clocks": clocks.summary()}
@@ -509,6 +510,20 @@ def e2e_pipelined(sess, hp, stream, steps, dist):
 
     pipeline(1)  # warm-up
     torch.cuda.synchronize()
+    # the box's copy rates alone (one gradient upload, one weight download),
+    # which bound the pipelined step when they are below ~100 GB/s
+    # (three of each: the rate of a shared host link dips now and then)
+    rates = {}
+    for name, dst, src in (("h2d_gbs", g_dev[1], g_host), ("d2h_gbs", q_host[0], sess.q)):
+        rates[name] = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(cs_in):
+                a.record(cs_in)
+                dst.copy_(src, non_blocking=True)
+                b.record(cs_in)
+            torch.cuda.synchronize()
+            rates[name].append(round(src.numel() * src.element_size() / (a.elapsed_time(b) * 1e6), 1))
     if dist:
         dist.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -516,7 +531,7 @@ def e2e_pipelined(sess, hp, stream, steps, dist):
     pipeline(steps, t0, t1)
     torch.cuda.synchronize()
     del g_dev[1]
-    return t0.elapsed_time(t1)
+    return t0.elapsed_time(t1), rates
 
 
 def _time_calls(fn, stream, reps: int = 3):

@@ -996,11 +996,11 @@ extern "C" hm_status mxfp8_scale_relayout(const uint8_t* src, uint8_t* dst, cons
             ra.rows[ra.n] = it.rows;
             ra.kb[ra.n] = it.kb;
             ra.block_rows[ra.n] = it.block_rows;
-            ra.flags[ra.n] = (((reinterpret_cast<uintptr_t>(src) + it.src_offset) % 4 == 0 && it.kb % 4 == 0)
-                                  ? hm::kRelayoutSrcWords
+            ra.flags[ra.n] = (((reinterpret_cast<uintptr_t>(src) + it.src_offset) % 16 == 0 && it.kb % 16 == 0)
+                                  ? hm::kRelayoutSrc16
                                   : 0) |
                              ((reinterpret_cast<uintptr_t>(dst) + it.dst_offset) % 16 == 0 ? hm::kRelayoutDst16 : 0);
-            ra.out_prefix[ra.n + 1] = ra.out_prefix[ra.n] + ((it.rows + 127) / 128) * ((it.kb + 3) / 4) * 512;
+            ra.work_prefix[ra.n + 1] = ra.work_prefix[ra.n] + ((it.rows + 127) / 128) * ((it.kb + 31) / 32);
             ra.n++;
         }
         if (!ra.n) continue;

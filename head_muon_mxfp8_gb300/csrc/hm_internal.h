@@ -123,7 +123,7 @@ constexpr int kMaxRelayoutItems = 32;
 struct RelayoutArgs {
     int32_t n;
     int32_t pad;
-    int64_t out_prefix[kMaxRelayoutItems + 1];  // exclusive prefix of output bytes
+    int64_t work_prefix[kMaxRelayoutItems + 1];  // exclusive prefix of 128-row x 32-column work units
     int64_t src[kMaxRelayoutItems];
     int64_t dst[kMaxRelayoutItems];
     int64_t rows[kMaxRelayoutItems];
@@ -131,7 +131,7 @@ struct RelayoutArgs {
     int32_t block_rows[kMaxRelayoutItems];
     int32_t flags[kMaxRelayoutItems];  // kRelayout* bits
 };
-constexpr int kRelayoutSrcWords = 1;  // src + src offset and kb are multiples of 4: 4-byte loads
+constexpr int kRelayoutSrc16 = 1;     // src + src offset and kb are multiples of 16: 16-byte row loads
 constexpr int kRelayoutDst16 = 2;     // dst + dst offset is 16-byte aligned: one 16-byte store per group
 
 // ---- launchers (return cudaGetLastError() of the launch) -----------------

@@ -94,53 +94,72 @@ __global__ void __launch_bounds__(128) requant_32x32_kernel(const __grid_constan
     }
 }
 
-// Each thread writes one 16-byte group of a tile: rows l, l+32, l+64, l+96
-// (l = group index within the tile) x 4 scale columns.
+// One CTA per work unit of 128 scale rows x 32 scale columns (eight 128 x 4
+// tiles side by side): the 256 threads first read the 4 KB block row by row
+// (two threads per row, 16 contiguous bytes each) into shared memory, then
+// each thread writes one 16-byte group of one tile -- rows l, l+32, l+64,
+// l+96 (l = group index within the tile) x 4 scale columns -- so the eight
+// tiles go out as 4 KB of contiguous stores.  Reading whole 32-byte sectors
+// of each scale row, instead of the 4 bytes one tile needs, is what keeps the
+// L2 from moving 8x the source bytes.
+constexpr int kRelayoutRowWords = 9;  // 32 bytes + 4 of padding per row: conflict-free column reads
+
 __global__ void __launch_bounds__(256) scale_relayout_kernel(const __grid_constant__ RelayoutArgs ra,
                                                               const uint8_t* __restrict__ src,
                                                               uint8_t* __restrict__ dst) {
-    const int64_t total = ra.out_prefix[ra.n] >> 4;
-    for (int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; o < total;
-         o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    __shared__ uint32_t S[128 * kRelayoutRowWords];
+    const int tid = threadIdx.x;
+    const int64_t total = ra.work_prefix[ra.n];
+    for (int64_t wu = blockIdx.x; wu < total; wu += gridDim.x) {
         int t = 0;
-        while ((ra.out_prefix[t + 1] >> 4) <= o) ++t;
-        const int64_t local = o - (ra.out_prefix[t] >> 4);  // 16-byte group index in this item
-        const int64_t ct = (ra.kb[t] + 3) >> 2;
-        const int64_t tile = local >> 5;
-        const int l = static_cast<int>(local & 31);
-        const int64_t r0 = (tile / ct) * 128 + l;
-        const int64_t c0 = (tile % ct) * 4;
+        while (ra.work_prefix[t + 1] <= wu) ++t;
+        const int64_t local = wu - ra.work_prefix[t];
         const int64_t kb = ra.kb[t];
-        // 4-byte source words when every scale row starts 4-byte aligned and
-        // the tile's 4 columns are all inside the row
-        const bool words = (ra.flags[t] & kRelayoutSrcWords) && c0 + 4 <= kb;
-        uint32_t word[4];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            const int64_t r = r0 + 32 * q4;
-            uint32_t v = 0;
-            if (r < ra.rows[t]) {
-                const uint8_t* row = src + ra.src[t] + (r / ra.block_rows[t]) * kb;
-                if (words) {
-                    v = __ldg(reinterpret_cast<const uint32_t*>(row + c0));
+        const int64_t ct = (kb + 3) >> 2;        // tiles across
+        const int64_t groups = (ct + 7) >> 3;    // work units across
+        const int64_t band = local / groups, J = local - band * groups;
+        // load: thread -> row rr of the band, 16 columns from 32J + 16h
+        {
+            const int rr = tid >> 1, h = tid & 1;
+            const int64_t r = band * 128 + rr;
+            const int64_t c0 = J * 32 + h * 16;
+            uint32_t wv[4] = {0u, 0u, 0u, 0u};
+            if (r < ra.rows[t] && c0 < kb) {
+                const uint8_t* row = src + ra.src[t] + (r / ra.block_rows[t]) * kb + c0;
+                if ((ra.flags[t] & kRelayoutSrc16) && c0 + 16 <= kb) {
+                    const uint4 x = __ldg(reinterpret_cast<const uint4*>(row));
+                    wv[0] = x.x; wv[1] = x.y; wv[2] = x.z; wv[3] = x.w;
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (c0 + c < kb) v |= static_cast<uint32_t>(row[c0 + c]) << (8 * c);
+                    for (int c = 0; c < 16; ++c)
+                        if (c0 + c < kb) wv[c >> 2] |= static_cast<uint32_t>(row[c]) << (8 * (c & 3));
                 }
             }
-            word[q4] = v;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) S[rr * kRelayoutRowWords + h * 4 + k] = wv[k];
         }
-        uint8_t* out = dst + ra.dst[t] + local * 16;
-        if (ra.flags[t] & kRelayoutDst16) {
-            *reinterpret_cast<uint4*>(out) = make_uint4(word[0], word[1], word[2], word[3]);
-        } else {
+        __syncthreads();
+        // store: thread -> tile jj of the eight, group l
+        {
+            const int jj = tid >> 5, l = tid & 31;
+            const int64_t j = J * 8 + jj;
+            if (j < ct) {
+                uint32_t word[4];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+                for (int q4 = 0; q4 < 4; ++q4) word[q4] = S[(l + 32 * q4) * kRelayoutRowWords + jj];
+                uint8_t* out = dst + ra.dst[t] + (band * ct + j) * 512 + l * 16;
+                if (ra.flags[t] & kRelayoutDst16) {
+                    *reinterpret_cast<uint4*>(out) = make_uint4(word[0], word[1], word[2], word[3]);
+                } else {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) out[q4 * 4 + c] = static_cast<uint8_t>(word[q4] >> (8 * c));
+                    for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) out[q4 * 4 + c] = static_cast<uint8_t>(word[q4] >> (8 * c));
+                    }
+                }
             }
         }
+        __syncthreads();
     }
 }
 
@@ -157,11 +176,10 @@ cudaError_t launch_requant_32x32(const ChainArgs& ch, const Mx32Args& ta, const 
 }
 
 cudaError_t launch_scale_relayout(const RelayoutArgs& ra, const uint8_t* src, uint8_t* dst, cudaStream_t st) {
-    const int64_t total = ra.out_prefix[ra.n];
+    const int64_t total = ra.work_prefix[ra.n];
     if (total == 0) return cudaSuccess;
-    const int64_t blocks = (total / 16 + 255) / 256;
     note_launch();
-    scale_relayout_kernel<<<resident_grid(scale_relayout_kernel, 256, blocks), 256, 0, st>>>(ra, src, dst);
+    scale_relayout_kernel<<<resident_grid(scale_relayout_kernel, 256, total), 256, 0, st>>>(ra, src, dst);
     return cudaGetLastError();
 }
 
