@@ -356,6 +356,7 @@ struct hm_muon_plan {
     int64_t staging_elems = 0;
     int n_straddling = 0, n_frag = 0;
     size_t off_seg = 0, off_gather = 0, off_f2 = 0, off_nsu = 0, off_ustage = 0, off_vstage = 0;
+    size_t off_pace = 0;  // two ints pacing the CTA-pair GEMMs (zeroed at upload, kept zero between launches)
     size_t ws_bytes = 0;
     // upload state
     char* ws = nullptr;
@@ -544,6 +545,7 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
     p->off_f0x = take(p->f0x_tab.size() * sizeof(Range));
     p->off_ustage = take(static_cast<size_t>(p->staging_elems) * 2);
     p->off_vstage = take(static_cast<size_t>(p->staging_elems) * 4);
+    p->off_pace = take(2 * sizeof(int32_t));
     for (NsClassDev& c : p->classes) {
         size_t xb = static_cast<size_t>(c.n_units) * c.mp * c.np * 2;
         size_t ab = static_cast<size_t>(c.n_units) * c.mp * c.mp * 2;
@@ -651,6 +653,7 @@ extern "C" hm_status muon_plan_upload(hm_muon_plan* p, void* workspace, size_t w
             put(p->classes[k].pair_off, p->pair_tab[k].data(), p->pair_tab[k].size() * 4) != cudaSuccess)
             return HM_ERR_CUDA;
     if (put(p->off_f0x, p->f0x_tab.data(), p->f0x_tab.size() * sizeof(Range)) != cudaSuccess) return HM_ERR_CUDA;
+    if (cudaMemsetAsync(ws + p->off_pace, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return HM_ERR_CUDA;
     p->maps.assign(p->classes.size(), ClassMaps{});
     for (size_t k = 0; k < p->classes.size(); ++k) {
         const NsClassDev& c = p->classes[k];
@@ -703,36 +706,17 @@ hm_status refresh_steps(const hm_muon_plan* p, const hm_muon_hparams* hp, cudaSt
 
 }  // namespace
 
-// CTA-pair GEMM over the units of one class, in one or more launches.  With
-// many waves in one launch the pairs drift apart, tiles that read the same
-// operand panel stop running together and operands larger than the L2 come
-// from DRAM several times over (measured on 16 units of 5120 x 20480: X X^T
-// read 15-21 GB and B X 25-35 GB per launch).  A launch boundary brings the
-// pairs back into step, so units whose X exceeds half the L2 run one per
-// launch for X X^T (its K is the long side: each panel is read for the whole
-// tile) and two per launch for B X (short K; two units halve the idle part of
-// the last wave).  Measured: 8.1 GB and 14.5 GB, 5 % less time.
-static cudaError_t launch_pair_units(const CUtensorMap& a, const CUtensorMap& b, hm::GemmParams g, int b_mn,
-                                     int64_t x_bytes, cudaStream_t s) {
-    static int l2_bytes[64] = {0};
+// L2 size of the current device (cached per device).
+static int64_t device_l2_bytes() {
+    static int cached[64] = {0};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!l2_bytes[dev] && cudaDeviceGetAttribute(&l2_bytes[dev], cudaDevAttrL2CacheSize, dev) != cudaSuccess)
-        return cudaErrorInvalidValue;
-    int per = g.units;
-    if (2 * x_bytes > l2_bytes[dev]) {
-        if (g.epi == hm::kEpiGram) per = 1;
-        else if (g.epi == hm::kEpiUpdate || g.epi == hm::kEpiFinal) per = 2;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 128 << 20;
+    if (!cached[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess || v <= 0) v = 128 << 20;
+        cached[dev] = v;
     }
-    const int n = g.units;
-    for (int u0 = 0; u0 < n; u0 += per) {
-        g.unit0 = u0;
-        g.units = std::min(per, n - u0);
-        cudaError_t r = hm::launch_ns_gemm_pair(a, b, g, b_mn, s);
-        if (r != cudaSuccess) return r;
-        g.inject_no_ready = 0;  // the failure-test hook stops the first launch only
-    }
-    return cudaSuccess;
+    return cached[dev];
 }
 
 extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs* b, const hm_muon_hparams* hp,
@@ -796,7 +780,6 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 hm::launch_ns_prepare(c, units_dev, b->u, u_stage, ws, s) != cudaSuccess)
                 return HM_ERR_CUDA;
             auto bf = [&](size_t off) { return reinterpret_cast<uint16_t*>(ws + off); };
-            const int64_t x_bytes = static_cast<int64_t>(c.mp) * c.np * 2;
             int cur = 0;
             for (int it = 0; it < hp->ns_steps; ++it) {
                 hm::GemmParams g1{};
@@ -804,6 +787,11 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g1.epi = hm::kEpiGram; g1.alpha = 1.f; g1.beta = 0.f;
                 g1.out = bf(c.a_off); g1.out_us = static_cast<int64_t>(c.mp) * c.mp; g1.ld_out = c.mp;
                 g1.err = hm::device_error_word();
+                // pair pacing where it pays: units whose X is larger than half the
+                // L2 (operand panels that drifting pairs would fetch from DRAM again);
+                // small units stay cached anyway and only lose time to the waits
+                const bool big_x = 2 * static_cast<int64_t>(c.mp) * c.np * 2 > device_l2_bytes();
+                g1.pace = big_x ? reinterpret_cast<int32_t*>(ws + p->off_pace) : nullptr;
                 g1.tile_tab = reinterpret_cast<const int32_t*>(ws + c.sym_off);
                 g1.tab_len = c.sym_tiles;
                 g1.sym = 1;
@@ -814,7 +802,7 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 if (pair) {
                     g1.tile_tab = reinterpret_cast<const int32_t*>(ws + c.pair_off);
                     g1.tab_len = c.pair_tiles;
-                    if (launch_pair_units(mp.x_a[cur], mp.x_a[cur], g1, 0, x_bytes, s) != cudaSuccess) return HM_ERR_CUDA;
+                    if (hm::launch_ns_gemm_pair(mp.x_a[cur], mp.x_a[cur], g1, 0, s) != cudaSuccess) return HM_ERR_CUDA;
                 } else if (hm::launch_ns_gemm(mp.x_a[cur], mp.x_b[cur], g1, mp.bn1, 0, s) != cudaSuccess) {
                     return HM_ERR_CUDA;
                 }
@@ -825,7 +813,7 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g2.epi = hm::kEpiPoly; g2.alpha = hp->ns_c; g2.beta = hp->ns_b;
                 g2.add = bf(c.a_off); g2.add_us = g1.out_us; g2.ld_add = c.mp;
                 g2.out = bf(c.b_off);
-                if (pair ? launch_pair_units(mp.a_a, mp.a_a, g2, 0, x_bytes, s) != cudaSuccess
+                if (pair ? hm::launch_ns_gemm_pair(mp.a_a, mp.a_a, g2, 0, s) != cudaSuccess
                          : hm::launch_ns_gemm(mp.a_a, mp.a_b, g2, mp.bn1, 0, s) != cudaSuccess)
                     return HM_ERR_CUDA;
 
@@ -839,9 +827,19 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g3.m_real = c.m; g3.n_real = c.n;
                 g3.group_m = c.mp / 128;  // column bands: each X panel is fetched once per unit
                 g3.err = g1.err;
+                g3.pace = g1.pace;
                 if (pair) {
-                    g3.group_m = (c.mp + 255) / 256;
-                    if (launch_pair_units(mp.b_a, mp.x_mn[cur], g3, 1, x_bytes, s) != cudaSuccess) return HM_ERR_CUDA;
+                    // B X raster for pairs: tile columns within bands of tile-rows, the
+                    // fewest equal bands whose slab of B fits in a quarter of the L2 --
+                    // that slab is re-read by every wave of its band and has to stay
+                    // resident (5120 x 20480 class: two bands, 10.3 GB read per launch
+                    // instead of 15.8 GB with one)
+                    const int tiles_m = (c.mp + 255) / 256;
+                    const int64_t b_bytes = static_cast<int64_t>(c.mp) * c.mp * 2;
+                    const int64_t cap = std::max<int64_t>(device_l2_bytes() / 4, 1);
+                    const int bands = static_cast<int>(std::min<int64_t>((b_bytes + cap - 1) / cap, tiles_m));
+                    g3.group_m = (tiles_m + bands - 1) / bands;
+                    if (hm::launch_ns_gemm_pair(mp.b_a, mp.x_mn[cur], g3, 1, s) != cudaSuccess) return HM_ERR_CUDA;
                 } else if (hm::launch_ns_gemm(mp.b_a, mp.x_mn[cur], g3, mp.bn3, 1, s) != cudaSuccess) {
                     return HM_ERR_CUDA;
                 }

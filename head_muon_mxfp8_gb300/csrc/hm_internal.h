@@ -97,7 +97,8 @@ struct GemmParams {
     int32_t sym;              // symmetric output: write (i, j) and (j, i) for j >= i only
     int32_t group_m;          // tile-rows per raster band of the full grid (0 = 8)
     int32_t inject_no_ready;  // failure test: never signal an accumulator as ready
-    int32_t unit0;            // index of the first unit this launch covers
+    int32_t* pace;            // CTA-pair kernel: 2 device ints (tiles issued, pairs done), zero between
+                              // launches; nullptr = pairs run unpaced
 };
 
 // chain geometry the device needs: z1 edges and the segment base of every chunk

@@ -207,6 +207,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
         }
     }
 }
+// Pacing of the CTA pairs.  Tiles are dealt round-robin, so in wave k every
+// pair works on its k-th tile and tiles that share an operand panel run at
+// the same time; left alone, pairs drift apart over many waves and those
+// panels come from DRAM again.  Each pair's producer counts the tiles whose
+// loads it has issued in pace[0] and, before its k-th tile, waits until
+// every pair has issued its (k-1)-th.  The wait only shapes timing: it gives
+// up after kPaceWaitNs and carries on, so it can neither hang nor change a
+// result.  The last pair to finish zeroes both counters for the next launch.
+constexpr unsigned long long kPaceWaitNs = 200000;  // 200 us
+
+__device__ __forceinline__ void pace_wait(const int32_t* issued, int target) {
+    if (*reinterpret_cast<const volatile int32_t*>(issued) >= target) return;
+    const unsigned long long t0 = globaltimer();
+    while (*reinterpret_cast<const volatile int32_t*>(issued) < target)
+        if (globaltimer() - t0 > kPaceWaitNs) return;
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
                                             int c2) {
     asm volatile(
@@ -299,7 +316,6 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, int& u, 
         const int32_t e = __ldg(p.tile_tab + (t - u * p.tab_len));
         tm = e >> 16;
         tn = e & 0xFFFF;
-        u += p.unit0;
         return;
     }
     const int per = p.tiles_m * p.tiles_n;
@@ -313,7 +329,6 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, int& u, 
     const int rr = r - g * group;
     tm = first + rr % gm;
     tn = rr / gm;
-    u += p.unit0;
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& x, float* f) {
@@ -745,9 +760,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int s = 0;
             uint32_t ph = 0, armed = 0, armed_par = 0;
             bool ok = true;
-            for (int t = pair; t < total && ok; t += npairs) {
+            int k_local = 0;
+            for (int t = pair; t < total && ok; t += npairs, ++k_local) {
                 int u, tm, tn;
                 decode_tile(t, p, u, tm, tn);
+                if (p.pace && leader && k_local > 0) pace_wait(p.pace, k_local * npairs);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, p.err, bail)) { ok = false; break; }
                     armed |= 1u << s;
@@ -764,6 +781,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tma_load_3d_pair(smem_u32(sb + s * C::B_BYTES), &tmb, fb, kb * BK, tn * C::BNP + rank * 128, u);
                     }
                     if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (p.pace && leader) atomicAdd(p.pace, 1);
+            }
+            if (p.pace && leader) {
+                // a pair that stopped early still counts its remaining tiles,
+                // so no other pair waits for them
+                for (int t = pair + k_local * npairs; t < total; t += npairs) atomicAdd(p.pace, 1);
+                if (atomicAdd(p.pace + 1, 1) == npairs - 1) {
+                    atomicExch(p.pace, 0);
+                    atomicExch(p.pace + 1, 0);
                 }
             }
             // the even CTA's full barriers count both CTAs' bytes: waiting on
