@@ -48,9 +48,12 @@ def ns_flops(cfg, steps: int) -> float:
 
 
 def ns_executed_flops(cfg, steps: int) -> float:
-    """Tensor-core FLOP the kernels actually issue per update: padded tiles
-    (128 x BN, K padded to 64), only the on-or-above-diagonal tiles of the
-    symmetric products A = X X^T and B = bA + cAA, the full grid of B X."""
+    """Tensor-core FLOP the kernels actually issue per update, by the kernel
+    a shape class runs on:
+    - m <= 128 (single-CTA GEMMs): 128 x 128 tiles on or above the diagonal
+      for X X^T and bA + cAA, 128 x BN tiles of B X, K padded to 64;
+    - m > 128 (CTA pairs): 256 x 256 tiles, the upper triangle for the
+      symmetric products and the full grid of B X."""
     classes = {}
     for u in cfg.units:
         key = (min(u.rows, u.cols), max(u.rows, u.cols))
@@ -58,12 +61,13 @@ def ns_executed_flops(cfg, steps: int) -> float:
     tot = 0.0
     for (m, n), cnt in classes.items():
         mp, np_ = -(-m // 128) * 128, -(-n // 64) * 64
-        bn1 = 256 if mp >= 256 else 128
-        bn3 = 256 if np_ >= 256 else 128
-        tiles_m, tiles_n1 = mp // 128, -(-mp // bn1)
-        sym = sum(1 for tm in range(tiles_m) for tn in range(tiles_n1) if tn * bn1 + bn1 - 1 >= tm * 128)
-        per_it = (sym * 2.0 * 128 * bn1 * np_ + sym * 2.0 * 128 * bn1 * mp +
-                  tiles_m * -(-np_ // bn3) * 2.0 * 128 * bn3 * mp)
+        if mp <= 128:
+            bn3 = 256 if np_ >= 256 else 128
+            per_it = 2.0 * 128 * 128 * np_ + 2.0 * 128 * 128 * mp + -(-np_ // bn3) * 2.0 * 128 * bn3 * mp
+        else:
+            t2 = -(-mp // 256)
+            tri = t2 * (t2 + 1) // 2
+            per_it = tri * 2.0 * 256 * 256 * (np_ + mp) + t2 * -(-np_ // 256) * 2.0 * 256 * 256 * mp
         tot += cnt * steps * per_it
     return tot
 
