@@ -431,10 +431,23 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                 if (i < p.m_real) {
 #pragma unroll
                     for (int k = 0; k < 32; ++k)
-                        if (j0 + k < p.n_real) dst[static_cast<int64_t>(j0 + k) * p.m_real + i] = stage[lane * 33 + k];
+                        if (j0 + k < p.n_real) __stcs(dst + static_cast<int64_t>(j0 + k) * p.m_real + i, stage[lane * 33 + k]);
+                }
+            } else if (j0 + 32 <= p.n_real && (p.n_real & 3) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+                // row-major v: 8 lanes per row, 16 bytes each, so every store covers
+                // 4 rows x 128 contiguous bytes; streaming stores, since v is read
+                // back only by f2 after the whole Newton-Schulz stage
+                const int c = (lane & 7) * 4;
+#pragma unroll 1
+                for (int s2 = 0; s2 < 8; ++s2) {
+                    const int r2 = s2 * 4 + (lane >> 3);
+                    const float* tv = stage + r2 * 33 + c;
+                    if (i0 + r2 < p.m_real)
+                        __stcs(reinterpret_cast<float4*>(dst + static_cast<int64_t>(i0 + r2) * p.n_real + j0 + c),
+                               make_float4(tv[0], tv[1], tv[2], tv[3]));
                 }
             } else if (j0 + lane < p.n_real) {
-                // row-major v: each store instruction writes 128 contiguous bytes of one row
+                // ragged or unaligned rows: one 4-byte store per lane, 128 bytes of one row per store
 #pragma unroll 4
                 for (int r2 = 0; r2 < 32; ++r2)
                     if (i0 + r2 < p.m_real) dst[static_cast<int64_t>(i0 + r2) * p.n_real + j0 + lane] = stage[r2 * 33 + lane];

@@ -314,3 +314,29 @@ def test_kernel_launch_count_of_one_fused_update(hm, dev, name):
     n = hm.hm_kernel_launches() - before
     torch.cuda.synchronize()
     assert n == 2 + s.info.n_classes * (3 + 3 * cfg.muon.ns_steps)
+
+
+def test_newton_schulz_ragged_row_tails(hm, dev):
+    """Units whose long side is not a multiple of 32 (n = 100, 72, 80): the
+    last 32-column chunk of v falls back from 16-byte to 4-byte stores, and
+    n = 100 / 80 rows are not 128-byte multiples.  Newton-Schulz output
+    against the oracle, and the guard words around every segment intact."""
+    cfg = workloads.scaled_muon("ragged_n", [(64, 100, None), (32, 72, None), (48, 80, None), (100, 64, None)],
+                                so=4, sw=2, sg=2)
+    data = workloads.generate(cfg, seed=13)
+    s = _session(cfg, dev)
+    s.load("w", data["w"])
+    s.load("g", data["g"])
+    s.load("m", np.zeros_like(data["w"]))
+    hp = _hp(cfg.muon)
+    s.run(hp, hm.HM_STAGE_F0 | hm.HM_STAGE_GATHER | hm.HM_STAGE_NS)
+    torch.cuda.synchronize()
+    u1 = s.fetch("u").numpy().view(np.uint16)
+    v = s.fetch("v").numpy()
+    for i, un in enumerate(cfg.units):
+        if not hm.muon_plan_unit(s.plan, i)["local"]:
+            v[un.offset:un.offset + un.numel] = s.staging(i)[1].cpu().numpy()
+    check_ns(cfg, u1, v, cfg.muon)
+    assert all(s.canary_intact().values())
+    assert hm.hm_device_error() == 0
+    s.close()
