@@ -103,7 +103,11 @@ __global__ void __launch_bounds__(256) ns_prepare_kernel(const NsUnit* __restric
                                                           const uint16_t* __restrict__ u_stage,
                                                           const float* __restrict__ inv, uint16_t* __restrict__ X,
                                                           int m, int n, int np) {
-    __shared__ __align__(16) uint16_t T[64][72];  // X orientation; 144-byte rows keep 16-byte alignment
+    // X orientation.  The 8-element chunk c of row r sits at chunk c ^ (r / 8):
+    // the transposed path writes down a column, and without the swizzle the 8
+    // rows r, r + 8, .. its lanes hit would share one bank
+    __shared__ __align__(16) uint16_t T[64][64];
+    auto tx = [](int r, int c) { return ((((c >> 3) ^ (r >> 3)) & 7) << 3) | (c & 7); };
     const int unit = blockIdx.z;
     const NsUnit nu = units[unit];
     const uint16_t* src = ((nu.flags & kNsUStaged) ? u_stage : u_root) + nu.u_off;
@@ -134,11 +138,11 @@ __global__ void __launch_bounds__(256) ns_prepare_kernel(const NsUnit* __restric
                 e[k] = (ur < rlim && uc + k < clim) ? scale_bf16(src[static_cast<int64_t>(ur) * ld + uc + k], s) : 0;
         }
         if (!tr) {
-            *reinterpret_cast<uint4*>(&T[a][b0]) = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16),
+            *reinterpret_cast<uint4*>(&T[a][tx(a, b0)]) = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16),
                                                               e[4] | (e[5] << 16), e[6] | (e[7] << 16));
         } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) T[b0 + k][a] = e[k];
+            for (int k = 0; k < 8; ++k) T[b0 + k][tx(b0 + k, a)] = e[k];
         }
     }
     __syncthreads();
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(256) ns_prepare_kernel(const NsUnit* __restric
     for (int v = threadIdx.x; v < 512; v += 256) {
         const int ii = v >> 3, jj = (v & 7) * 8;
         *reinterpret_cast<uint4*>(xo + static_cast<int64_t>(i0 + ii) * np + j0 + jj) =
-            *reinterpret_cast<const uint4*>(&T[ii][jj]);
+            *reinterpret_cast<const uint4*>(&T[ii][tx(ii, jj)]);
     }
 }
 
