@@ -275,6 +275,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// After tmem_ld_wait: makes every later use of r depend on a point after the
+// wait, so the compiler cannot read registers a tcgen05.ld is still filling.
+__device__ __forceinline__ void tmem_ld_pin(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
 
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA
 // with the 128-byte swizzle: rows of 64 bf16 (128 B), 8-row atoms of 1024 B
@@ -377,15 +387,22 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                                               float* stage, int half, uint4 (&next)[4]) {
     const int i = i_base + row;
     const int c_end = (half + 1) * (BN / 64);
+    // the next chunk's TMEM load is in flight while the current chunk is processed
+    uint32_t rn[32];
+    __syncwarp();
+    tmem_ld32(taddr + half * (BN / 64) * 32, rn);
 #pragma unroll 1
     for (int c = half * (BN / 64); c < c_end; ++c) {
         const int j0 = tn * BN + c * 32;
         uint4 a[4] = {next[0], next[1], next[2], next[3]};
         if (addend_coalesced(p) && c + 1 < c_end) load_addend_chunk(p, u, i - (threadIdx.x & 31), j0 + 32, next);
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(taddr + c * 32, r);
         tmem_ld_wait();
+        tmem_ld_pin(rn);
+        uint32_t r[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = rn[k];
+        __syncwarp();
+        if (c + 1 < c_end) tmem_ld32(taddr + (c + 1) * 32, rn);
         if (j0 >= p.N) continue;  // warp-uniform; N is a multiple of 32
         const int i0 = i - (threadIdx.x & 31);  // first row of this warp
         if (p.sym && j0 + 32 <= i0) continue;   // symmetric output: chunk below the diagonal
