@@ -98,11 +98,13 @@ __device__ __forceinline__ uint16_t scale_bf16(uint16_t raw, float s) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(static_cast<uint32_t>(raw) << 16) * s));
 }
 
-__global__ void __launch_bounds__(256) ns_prepare_kernel(const NsUnit* __restrict__ units,
-                                                          const uint16_t* __restrict__ u_root,
-                                                          const uint16_t* __restrict__ u_stage,
-                                                          const float* __restrict__ inv, uint16_t* __restrict__ X,
-                                                          int m, int n, int np) {
+constexpr int kPrepThreads = 128;  // 4 of the tile's 512 16-byte chunks per thread, loads first
+
+__global__ void __launch_bounds__(kPrepThreads) ns_prepare_kernel(const NsUnit* __restrict__ units,
+                                                                   const uint16_t* __restrict__ u_root,
+                                                                   const uint16_t* __restrict__ u_stage,
+                                                                   const float* __restrict__ inv,
+                                                                   uint16_t* __restrict__ X, int m, int n, int np) {
     // X orientation.  The 8-element chunk c of row r sits at chunk c ^ (r / 8):
     // the transposed path writes down a column, and without the swizzle the 8
     // rows r, r + 8, .. its lanes hit would share one bank
@@ -118,36 +120,47 @@ __global__ void __launch_bounds__(256) ns_prepare_kernel(const NsUnit* __restric
     // 64 consecutive u entries of one u row (non-transposed) or of one u column
     const int ld = tr ? m : n;
     const bool vec_ok = (ld & 7) == 0;
-    for (int v = threadIdx.x; v < 512; v += 256) {
+    const int rlim = tr ? n : m, clim = tr ? m : n;
+    uint4 raw[4];  // 8 bf16 of u per chunk, zero outside the unit
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int v = threadIdx.x + t * kPrepThreads;
         const int a = v >> 3, b0 = (v & 7) * 8;  // u-tile row a, 8 entries from b0
         // non-transposed: u row i0+a, cols j0+b0..; transposed: u row j0+a, cols i0+b0..
         const int ur = (tr ? j0 : i0) + a, uc = (tr ? i0 : j0) + b0;
-        const int rlim = tr ? n : m, clim = tr ? m : n;
-        uint16_t e[8];
         if (ur < rlim && vec_ok && uc + 8 <= clim) {
-            const uint4 x = __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(ur) * ld + uc));
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                e[2 * k] = scale_bf16(static_cast<uint16_t>(w[k] & 0xFFFFu), s);
-                e[2 * k + 1] = scale_bf16(static_cast<uint16_t>(w[k] >> 16), s);
-            }
+            raw[t] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(ur) * ld + uc));
         } else {
+            uint32_t h[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                e[k] = (ur < rlim && uc + k < clim) ? scale_bf16(src[static_cast<int64_t>(ur) * ld + uc + k], s) : 0;
+            for (int k = 0; k < 8; ++k) h[k] = (ur < rlim && uc + k < clim) ? src[static_cast<int64_t>(ur) * ld + uc + k] : 0u;
+            raw[t] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int v = threadIdx.x + t * kPrepThreads;
+        const int a = v >> 3, b0 = (v & 7) * 8;
+        const uint32_t w[4] = {raw[t].x, raw[t].y, raw[t].z, raw[t].w};
+        uint32_t e[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            e[2 * k] = scale_bf16(static_cast<uint16_t>(w[k] & 0xFFFFu), s);
+            e[2 * k + 1] = scale_bf16(static_cast<uint16_t>(w[k] >> 16), s);
         }
         if (!tr) {
-            *reinterpret_cast<uint4*>(&T[a][tx(a, b0)]) = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16),
-                                                              e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+            *reinterpret_cast<uint4*>(&T[a][tx(a, b0)]) =
+                make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
         } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) T[b0 + k][tx(b0 + k, a)] = e[k];
+            for (int k = 0; k < 8; ++k) T[b0 + k][tx(b0 + k, a)] = static_cast<uint16_t>(e[k]);
         }
     }
     __syncthreads();
     uint16_t* xo = X + static_cast<int64_t>(unit) * gridDim.y * 64 * np;
-    for (int v = threadIdx.x; v < 512; v += 256) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int v = threadIdx.x + t * kPrepThreads;
         const int ii = v >> 3, jj = (v & 7) * 8;
         *reinterpret_cast<uint4*>(xo + static_cast<int64_t>(i0 + ii) * np + j0 + jj) =
             *reinterpret_cast<const uint4*>(&T[ii][tx(ii, jj)]);
@@ -982,8 +995,9 @@ cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, cons
                               const uint16_t* u_stage, char* ws, cudaStream_t st) {
     dim3 g(c.np / 64, c.mp / 64, c.n_units);
     note_launch();
-    ns_prepare_kernel<<<g, 256, 0, st>>>(units_dev, u_root, u_stage, reinterpret_cast<const float*>(ws + c.inv_off),
-                                         reinterpret_cast<uint16_t*>(ws + c.x_off[0]), c.m, c.n, c.np);
+    ns_prepare_kernel<<<g, kPrepThreads, 0, st>>>(units_dev, u_root, u_stage,
+                                                  reinterpret_cast<const float*>(ws + c.inv_off),
+                                                  reinterpret_cast<uint16_t*>(ws + c.x_off[0]), c.m, c.n, c.np);
     return cudaGetLastError();
 }
 
