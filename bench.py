@@ -359,6 +359,31 @@ def run_ours(args, cfg):
     ms_per_step = ms / args.steps
     value = whole_job_rate(world, cfg.numel, args.steps, ms)
 
+    # ---- optional: the same fused step captured once in a CUDA graph and
+    # replayed (no per-kernel launch cost; matters for small workloads) ----
+    graph = None
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            sess.run(hp, abi.HM_STAGE_ALL_FUSED, stream)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                g.replay()
+            ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ga.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            gb.record(stream)
+        torch.cuda.synchronize()
+        if abi.hm_device_error() != 0:
+            raise RuntimeError("device error word set during graph replay")
+        gms = max_over_ranks(ga.elapsed_time(gb), dist, dev)
+        graph = {"value": whole_job_rate(world, cfg.numel, args.steps, gms), "unit": UNIT,
+                 "ms_per_step": gms / args.steps,
+                 "note": "one fused update captured in a CUDA graph, replayed steps times"}
+        del g
+
     # ---- end to end: host gradient in, host MXFP8 runtime weight out -----
     e2e_steps = max(2, min(4, args.steps))
     e2e_ms, copy_rates = e2e_pipelined(sess, hp, stream, e2e_steps, dist)
@@ -440,6 +465,8 @@ def run_ours(args, cfg):
                         "note": "host gradient in, host MXFP8 weights + scales out, every step; copies on their own "
                                 "streams overlap the previous / next step's Newton-Schulz stage"},
                 "gpu_launches": launches, "clocks": clocks.summary()}
+        if graph is not None:
+            line["graph"] = graph
         print(json.dumps(line), flush=True)
     sess.close()
     if dist:
@@ -635,6 +662,7 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-adamw", action="store_true")
     ap.add_argument("--skip-extra", action="store_true", help="skip the 32x32 / relayout / reduce-scatter timings")
+    ap.add_argument("--graph", action="store_true", help="also time the fused step replayed from a CUDA graph")
     args = ap.parse_args()
     cfg = workloads.get(args.workload)
     if cfg.optimizer != "muon":
