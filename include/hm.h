@@ -224,7 +224,13 @@ typedef struct {  /* device roots, each in the chain's emulated layout */
  * straddling units live in the workspace staging; v of local units is
  * written to the v root at the unit's own offsets.  A plan serves one stream
  * at a time: calls on one plan must not run concurrently (they share the
- * workspace and the plan's cached per-unit steps). */
+ * workspace and the plan's cached per-unit steps).
+ * Allocates nothing and launches only kernels on `stream`, so a call can be
+ * captured into a CUDA graph and replayed, provided one call with the same
+ * lr and alpha_mode ran outside the capture first: a change of either
+ * re-uploads the per-unit step table from host memory (a copy a capture
+ * cannot hold).  Replays read that table from the workspace, so a later
+ * uncaptured call with a new lr also updates the graph's steps. */
 hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs* bufs,
                             const hm_muon_hparams* hp, void* workspace, size_t workspace_bytes,
                             int stages, void* stream);
