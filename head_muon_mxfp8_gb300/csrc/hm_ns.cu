@@ -419,17 +419,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
         if (j0 >= p.N) continue;  // warp-uniform; N is a multiple of 32
         const int i0 = i - (threadIdx.x & 31);  // first row of this warp
         if (p.sym && j0 + 32 <= i0) continue;   // symmetric output: chunk below the diagonal
-        float v[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * p.alpha;
         if ((p.epi == kEpiUpdate || p.epi == kEpiFinal) && !p.sym) {
             // aX + BX through the warp's staging: the lane that holds row i parks
             // its 32 sums, then every load of the addend (and every store of X')
             // covers 8 rows x 64 contiguous bytes, 4 lanes per row, instead of
-            // 32 rows x 16 bytes
+            // 32 rows x 16 bytes.  The 32 x 32 fp32 tile keeps 16-byte chunk c of
+            // row r at chunk c ^ (r % 8), so the row-wise writes and the 4-lanes-
+            // per-row reads are both conflict-free 16-byte accesses.  (These two
+            // epilogues have no alpha: acc is B X as it stands.)
             const int lane = threadIdx.x & 31;
+            auto st4 = [&](int r, int c4) { return reinterpret_cast<float4*>(stage + r * 32 + ((c4 ^ (r & 7)) << 2)); };
 #pragma unroll
-            for (int k = 0; k < 32; ++k) stage[lane * 33 + k] = v[k];
+            for (int c4 = 0; c4 < 8; ++c4)
+                *st4(lane, c4) = make_float4(__uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]),
+                                             __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3]));
             __syncwarp();
             const int cq = (lane & 3) * 8;
             if (p.epi == kEpiUpdate) {
@@ -439,8 +442,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                     const int rr = (lane >> 2) + 8 * s;
                     float a8[8], o[8];
                     unpack_bf16x8(a[s], a8);
+                    const float4 y0 = *st4(rr, cq >> 2), y1 = *st4(rr, (cq >> 2) + 1);
+                    const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) o[t] = fmaf(p.beta, a8[t], stage[rr * 33 + cq + t]);
+                    for (int t = 0; t < 8; ++t) o[t] = fmaf(p.beta, a8[t], y[t]);
                     *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(i0 + rr) * p.ld_out) = make_uint4(
                         bf16_bits(o[0]) | (bf16_bits(o[1]) << 16), bf16_bits(o[2]) | (bf16_bits(o[3]) << 16),
                         bf16_bits(o[4]) | (bf16_bits(o[5]) << 16), bf16_bits(o[6]) | (bf16_bits(o[7]) << 16));
@@ -453,8 +458,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                 const int rr = (lane >> 2) + 8 * s;
                 float a8[8];
                 unpack_bf16x8(a[s], a8);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) stage[rr * 33 + cq + t] = fmaf(p.beta, a8[t], stage[rr * 33 + cq + t]);
+                float4* p0 = st4(rr, cq >> 2);
+                float4* p1 = st4(rr, (cq >> 2) + 1);
+                const float4 y0 = *p0, y1 = *p1;
+                *p0 = make_float4(fmaf(p.beta, a8[0], y0.x), fmaf(p.beta, a8[1], y0.y), fmaf(p.beta, a8[2], y0.z),
+                                  fmaf(p.beta, a8[3], y0.w));
+                *p1 = make_float4(fmaf(p.beta, a8[4], y1.x), fmaf(p.beta, a8[5], y1.y), fmaf(p.beta, a8[6], y1.z),
+                                  fmaf(p.beta, a8[7], y1.w));
             }
             __syncwarp();
             const NsUnit nu = p.ns_units[u];
@@ -464,31 +474,41 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                 // of v's row j0 + k
                 if (i < p.m_real) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        if (j0 + k < p.n_real) __stcs(dst + static_cast<int64_t>(j0 + k) * p.m_real + i, stage[lane * 33 + k]);
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 y = *st4(lane, c4);
+                        const float yk[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (j0 + 4 * c4 + e < p.n_real)
+                                __stcs(dst + static_cast<int64_t>(j0 + 4 * c4 + e) * p.m_real + i, yk[e]);
+                    }
                 }
             } else if (j0 + 32 <= p.n_real && (p.n_real & 3) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
                 // row-major v: 8 lanes per row, 16 bytes each, so every store covers
                 // 4 rows x 128 contiguous bytes; streaming stores, since v is read
                 // back only by f2 after the whole Newton-Schulz stage
-                const int c = (lane & 7) * 4;
+                const int c4 = lane & 7;
 #pragma unroll 1
                 for (int s2 = 0; s2 < 8; ++s2) {
                     const int r2 = s2 * 4 + (lane >> 3);
-                    const float* tv = stage + r2 * 33 + c;
                     if (i0 + r2 < p.m_real)
-                        __stcs(reinterpret_cast<float4*>(dst + static_cast<int64_t>(i0 + r2) * p.n_real + j0 + c),
-                               make_float4(tv[0], tv[1], tv[2], tv[3]));
+                        __stcs(reinterpret_cast<float4*>(dst + static_cast<int64_t>(i0 + r2) * p.n_real + j0 + 4 * c4),
+                               *st4(r2, c4));
                 }
             } else if (j0 + lane < p.n_real) {
                 // ragged or unaligned rows: one 4-byte store per lane, 128 bytes of one row per store
 #pragma unroll 4
                 for (int r2 = 0; r2 < 32; ++r2)
-                    if (i0 + r2 < p.m_real) dst[static_cast<int64_t>(i0 + r2) * p.n_real + j0 + lane] = stage[r2 * 33 + lane];
+                    if (i0 + r2 < p.m_real)
+                        dst[static_cast<int64_t>(i0 + r2) * p.n_real + j0 + lane] =
+                            stage[r2 * 32 + ((((lane >> 2) ^ (r2 & 7)) << 2) | (lane & 3))];
             }
             __syncwarp();
             continue;
         }
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * p.alpha;
         if (p.epi == kEpiPoly) {
             const uint4* ap = reinterpret_cast<const uint4*>(p.add + u * p.add_us + static_cast<int64_t>(i) * p.ld_add + j0);
 #pragma unroll

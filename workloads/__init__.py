@@ -192,6 +192,16 @@ def video_dit(layers: int = 8) -> Config:
                   "muon", b.members, b.units, so=32, sw=16, sg=16)
 
 
+def video_dit_layer() -> Config:
+    """One Video-DiT layer (120 heads, fc1, fc2; 288 M parameters): the same
+    shape classes at one eighth of the size, for profiling captures that must
+    stay a few GB on the device."""
+    c = video_dit(layers=1)
+    return Config("video_dit_layer", "1 layer of video_dit: hidden 5120, 120 per-head 128x5120 units, "
+                  "fc1 [20480][5120] + fc2 [5120][20480]; 32 emulated ranks",
+                  "muon", c.members, c.units, so=c.so, sw=c.sw, sg=c.sg)
+
+
 def scaled_muon(name: str, shapes: List[Tuple[int, int, Optional[int]]], so: int,
                 sw: int, sg: int) -> Config:
     """A free-form Muon config for tests: (rows, cols, unit_rows or None)."""
@@ -207,6 +217,7 @@ CONFIGS = {
     "lm_layer": lm_layer,
     "moe_layer": moe_layer,
     "video_dit": video_dit,
+    "video_dit_layer": video_dit_layer,
 }
 
 
