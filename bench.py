@@ -79,7 +79,7 @@ def straddling_elems(cfg, plan_info) -> int:
 # DRAM bytes (read + write) of one Newton-Schulz stage of the Video-DiT x8
 # workload, from profiles/video_dit_launch_list_dram.md, valid for the kernel
 # source it was measured on (sha256 prefix of hm_ns.cu).
-NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.649e+11, "hm_ns_sha256": "8f75f3d7e3e02830"}
+NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.657e+11, "hm_ns_sha256": "bb7a4dd6c3c9d059"}
 
 
 def ns_stage_traffic(cfg):

@@ -370,7 +370,7 @@ __device__ __forceinline__ uint32_t bf16_bits(float x) { return __bfloat16_as_us
 
 // Epilogues that add aX read the addend with 4 lanes per row (see below).
 __device__ __forceinline__ bool addend_coalesced(const GemmParams& p) {
-    return (p.epi == kEpiUpdate || p.epi == kEpiFinal) && !p.sym;
+    return ((p.epi == kEpiUpdate || p.epi == kEpiFinal) && !p.sym) || (p.epi == kEpiPoly && p.sym);
 }
 
 // With a short K (B X of the 128-row head class: two k-blocks) the epilogue,
@@ -506,6 +506,81 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
             __syncwarp();
             continue;
         }
+        if (p.sym) {
+            // symmetric output (A = X X^T, B = bA + cAA): this warp owns rows
+            // i0..i0+31 and writes only elements with j >= i, each to (i, j) and
+            // to (j, i), through the same swizzled staging tile: the chunk and its
+            // transpose both leave as 16-byte stores of 8 rows x 16 bytes
+            const int lane = threadIdx.x & 31;
+            auto st4 = [&](int r, int c4) { return reinterpret_cast<float4*>(stage + r * 32 + ((c4 ^ (r & 7)) << 2)); };
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+                *st4(lane, c4) = make_float4(__uint_as_float(r[4 * c4]) * p.alpha, __uint_as_float(r[4 * c4 + 1]) * p.alpha,
+                                             __uint_as_float(r[4 * c4 + 2]) * p.alpha,
+                                             __uint_as_float(r[4 * c4 + 3]) * p.alpha);
+            __syncwarp();
+            const int cq = (lane & 3) * 8;
+            if (p.epi == kEpiPoly) {
+                // + b A, A read 4 lanes per row (prefetched like the aX addend)
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const int rr = (lane >> 2) + 8 * s;
+                    float a8[8];
+                    unpack_bf16x8(a[s], a8);
+                    float4* p0 = st4(rr, cq >> 2);
+                    float4* p1 = st4(rr, (cq >> 2) + 1);
+                    const float4 y0 = *p0, y1 = *p1;
+                    *p0 = make_float4(fmaf(p.beta, a8[0], y0.x), fmaf(p.beta, a8[1], y0.y), fmaf(p.beta, a8[2], y0.z),
+                                      fmaf(p.beta, a8[3], y0.w));
+                    *p1 = make_float4(fmaf(p.beta, a8[4], y1.x), fmaf(p.beta, a8[5], y1.y), fmaf(p.beta, a8[6], y1.z),
+                                      fmaf(p.beta, a8[7], y1.w));
+                }
+                __syncwarp();
+            }
+            uint16_t* ob = p.out + u * p.out_us;
+            if (j0 == i0) {
+                // the diagonal 32 x 32 block, element by element
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 y = *st4(lane, c4);
+                    const float yk[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = 4 * c4 + e;
+                        if (k >= lane) {
+                            const uint16_t bv = static_cast<uint16_t>(bf16_bits(yk[e]));
+                            ob[static_cast<int64_t>(i0 + lane) * p.ld_out + j0 + k] = bv;
+                            ob[static_cast<int64_t>(j0 + k) * p.ld_out + i0 + lane] = bv;
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const int rr = (lane >> 2) + 8 * s;
+                    const float4 y0 = *st4(rr, cq >> 2), y1 = *st4(rr, (cq >> 2) + 1);
+                    *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(i0 + rr) * p.ld_out + j0 + cq) = make_uint4(
+                        bf16_bits(y0.x) | (bf16_bits(y0.y) << 16), bf16_bits(y0.z) | (bf16_bits(y0.w) << 16),
+                        bf16_bits(y1.x) | (bf16_bits(y1.y) << 16), bf16_bits(y1.z) | (bf16_bits(y1.w) << 16));
+                }
+                // mirror: row j0 + kk of the output takes column kk of the chunk,
+                // 8 of its rows per lane
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const int kk = (lane >> 2) + 8 * s;
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        y[e] = stage[(cq + e) * 32 + ((((kk >> 2) ^ e) << 2) | (kk & 3))];
+                    *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(j0 + kk) * p.ld_out + i0 + cq) = make_uint4(
+                        bf16_bits(y[0]) | (bf16_bits(y[1]) << 16), bf16_bits(y[2]) | (bf16_bits(y[3]) << 16),
+                        bf16_bits(y[4]) | (bf16_bits(y[5]) << 16), bf16_bits(y[6]) | (bf16_bits(y[7]) << 16));
+                }
+            }
+            __syncwarp();
+            continue;
+        }
+        // full-grid outputs (the allocation-free entry point's A and B)
         float v[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * p.alpha;
@@ -519,21 +594,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                 for (int k = 0; k < 8; ++k) v[q * 8 + k] = fmaf(p.beta, a8[k], v[q * 8 + k]);
             }
         }
-        if (p.sym) {
-            // symmetric output: this warp owns rows i0..i0+31; only elements
-            // with j >= i are written, each to (i, j) and (j, i)
-            uint16_t* ob = p.out + u * p.out_us;
-            if (j0 < i0 + 32) {                            // the diagonal 32 x 32 block
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if (j0 + k >= i) {
-                        const uint16_t b = static_cast<uint16_t>(bf16_bits(v[k]));
-                        ob[static_cast<int64_t>(i) * p.ld_out + j0 + k] = b;
-                        ob[static_cast<int64_t>(j0 + k) * p.ld_out + i] = b;
-                    }
-                continue;
-            }
-        }
         uint4 pk[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -544,14 +604,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
         uint4* op = reinterpret_cast<uint4*>(p.out + u * p.out_us + static_cast<int64_t>(i) * p.ld_out + j0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) op[q] = pk[q];
-        if (p.sym) {
-            // the mirror half of a symmetric output: (j, i) for every (i, j) above
-            uint16_t* tp = p.out + u * p.out_us + static_cast<int64_t>(j0) * p.ld_out + i;
-            const uint32_t* w = reinterpret_cast<const uint32_t*>(pk);
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-                tp[static_cast<int64_t>(k) * p.ld_out] = static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
-        }
     }
 }
 
