@@ -998,7 +998,7 @@ extern "C" hm_status mxfp8_scale_relayout(const uint8_t* src, uint8_t* dst, cons
                                   ? hm::kRelayoutSrc16
                                   : 0) |
                              ((reinterpret_cast<uintptr_t>(dst) + it.dst_offset) % 16 == 0 ? hm::kRelayoutDst16 : 0);
-            ra.work_prefix[ra.n + 1] = ra.work_prefix[ra.n] + ((it.rows + 127) / 128) * ((it.kb + 31) / 32);
+            ra.work_prefix[ra.n + 1] = ra.work_prefix[ra.n] + ((it.rows + 127) / 128) * ((it.kb + 159) / 160);
             ra.n++;
         }
         if (!ra.n) continue;

@@ -124,7 +124,7 @@ constexpr int kMaxRelayoutItems = 32;
 struct RelayoutArgs {
     int32_t n;
     int32_t pad;
-    int64_t work_prefix[kMaxRelayoutItems + 1];  // exclusive prefix of 128-row x 32-column work units
+    int64_t work_prefix[kMaxRelayoutItems + 1];  // exclusive prefix of 128-row x 160-column work units
     int64_t src[kMaxRelayoutItems];
     int64_t dst[kMaxRelayoutItems];
     int64_t rows[kMaxRelayoutItems];

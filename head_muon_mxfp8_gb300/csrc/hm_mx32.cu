@@ -94,15 +94,17 @@ __global__ void __launch_bounds__(128) requant_32x32_kernel(const __grid_constan
     }
 }
 
-// One CTA per work unit of 128 scale rows x 32 scale columns (eight 128 x 4
-// tiles side by side): the 256 threads first read the 4 KB block row by row
-// (two threads per row, 16 contiguous bytes each) into shared memory, then
-// each thread writes one 16-byte group of one tile -- rows l, l+32, l+64,
-// l+96 (l = group index within the tile) x 4 scale columns -- so the eight
-// tiles go out as 4 KB of contiguous stores.  Reading whole 32-byte sectors
-// of each scale row, instead of the 4 bytes one tile needs, is what keeps the
-// L2 from moving 8x the source bytes.
-constexpr int kRelayoutRowWords = 9;  // 32 bytes + 4 of padding per row: conflict-free column reads
+// Work units of 128 scale rows x 160 scale columns (forty 128 x 4 tiles side
+// by side).  The 256 threads read the unit's rows as 16-byte pieces (five per
+// thread, all in flight; a 160-byte row is a whole scale row of a K = 5120
+// tensor, so the unit is one contiguous 20 KB block) into shared memory,
+// then write one 16-byte group each of the forty tiles -- rows l, l+32,
+// l+64, l+96 of a tile (l = group index) x its 4 scale columns -- so the
+// unit leaves as 20 KB of contiguous stores.
+constexpr int kRelayoutCols = 160;                      // scale columns per work unit
+constexpr int kRelayoutTiles = kRelayoutCols / 4;       // 40 tiles
+constexpr int kRelayoutRowWords = kRelayoutCols / 4 + 1;  // 41: odd stride, conflict-free column reads
+constexpr int kRelayoutPieces = 128 * kRelayoutCols / 16 / 256;  // 16-byte loads per thread: 5
 
 __global__ void __launch_bounds__(256) scale_relayout_kernel(const __grid_constant__ RelayoutArgs ra,
                                                               const uint8_t* __restrict__ src,
@@ -111,51 +113,67 @@ __global__ void __launch_bounds__(256) scale_relayout_kernel(const __grid_consta
     const int tid = threadIdx.x;
     const int64_t total = ra.work_prefix[ra.n];
     for (int64_t wu = blockIdx.x; wu < total; wu += gridDim.x) {
-        int t = 0;
-        while (ra.work_prefix[t + 1] <= wu) ++t;
+        int lo = 0, hi = ra.n - 1;  // the item holding work unit wu
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ra.work_prefix[mid] <= wu) lo = mid;
+            else hi = mid - 1;
+        }
+        const int t = lo;
         const int64_t local = wu - ra.work_prefix[t];
         const int64_t kb = ra.kb[t];
-        const int64_t ct = (kb + 3) >> 2;        // tiles across
-        const int64_t groups = (ct + 7) >> 3;    // work units across
+        const int64_t ct = (kb + 3) >> 2;                                 // tiles across
+        const int64_t groups = (ct + kRelayoutTiles - 1) / kRelayoutTiles;  // work units across
         const int64_t band = local / groups, J = local - band * groups;
-        // load: thread -> row rr of the band, 16 columns from 32J + 16h
-        {
-            const int rr = tid >> 1, h = tid & 1;
+        const bool vec = (ra.flags[t] & kRelayoutSrc16) != 0;
+        // load: piece p -> row p / 10, 16 bytes from column 160 J + 16 (p % 10)
+        uint32_t wv[kRelayoutPieces][4];
+#pragma unroll
+        for (int k = 0; k < kRelayoutPieces; ++k) {
+            const int piece = tid + k * 256;
+            const int rr = piece / 10, part = piece % 10;
             const int64_t r = band * 128 + rr;
-            const int64_t c0 = J * 32 + h * 16;
-            uint32_t wv[4] = {0u, 0u, 0u, 0u};
+            const int64_t c0 = J * kRelayoutCols + part * 16;
+            wv[k][0] = wv[k][1] = wv[k][2] = wv[k][3] = 0u;
             if (r < ra.rows[t] && c0 < kb) {
                 const uint8_t* row = src + ra.src[t] + (r / ra.block_rows[t]) * kb + c0;
-                if ((ra.flags[t] & kRelayoutSrc16) && c0 + 16 <= kb) {
+                if (vec && c0 + 16 <= kb) {
                     const uint4 x = __ldg(reinterpret_cast<const uint4*>(row));
-                    wv[0] = x.x; wv[1] = x.y; wv[2] = x.z; wv[3] = x.w;
+                    wv[k][0] = x.x; wv[k][1] = x.y; wv[k][2] = x.z; wv[k][3] = x.w;
                 } else {
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
-                        if (c0 + c < kb) wv[c >> 2] |= static_cast<uint32_t>(row[c]) << (8 * (c & 3));
+                        if (c0 + c < kb) wv[k][c >> 2] |= static_cast<uint32_t>(row[c]) << (8 * (c & 3));
                 }
             }
+        }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) S[rr * kRelayoutRowWords + h * 4 + k] = wv[k];
+        for (int k = 0; k < kRelayoutPieces; ++k) {
+            const int piece = tid + k * 256;
+            const int rr = piece / 10, part = piece % 10;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) S[rr * kRelayoutRowWords + part * 4 + e] = wv[k][e];
         }
         __syncthreads();
-        // store: thread -> tile jj of the eight, group l
-        {
-            const int jj = tid >> 5, l = tid & 31;
-            const int64_t j = J * 8 + jj;
-            if (j < ct) {
-                uint32_t word[4];
+        // store: group g -> tile g / 32 of the forty, group l = g % 32 in it
+        uint8_t* out0 = dst + ra.dst[t] + (band * ct + J * kRelayoutTiles) * 512;
+        const bool dvec = (ra.flags[t] & kRelayoutDst16) != 0;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) word[q4] = S[(l + 32 * q4) * kRelayoutRowWords + jj];
-                uint8_t* out = dst + ra.dst[t] + (band * ct + j) * 512 + l * 16;
-                if (ra.flags[t] & kRelayoutDst16) {
-                    *reinterpret_cast<uint4*>(out) = make_uint4(word[0], word[1], word[2], word[3]);
-                } else {
+        for (int k = 0; k < kRelayoutPieces; ++k) {
+            const int g = tid + k * 256;
+            const int jj = g >> 5, l = g & 31;
+            if (J * kRelayoutTiles + jj >= ct) continue;
+            uint32_t word[4];
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q4 = 0; q4 < 4; ++q4) word[q4] = S[(l + 32 * q4) * kRelayoutRowWords + jj];
+            uint8_t* out = out0 + g * 16;
+            if (dvec) {
+                *reinterpret_cast<uint4*>(out) = make_uint4(word[0], word[1], word[2], word[3]);
+            } else {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) out[q4 * 4 + c] = static_cast<uint8_t>(word[q4] >> (8 * c));
-                    }
+                for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) out[q4 * 4 + c] = static_cast<uint8_t>(word[q4] >> (8 * c));
                 }
             }
         }

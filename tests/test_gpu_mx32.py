@@ -76,7 +76,9 @@ def test_scale_relayout_128x4(hm, dev):
     rng = np.random.default_rng(25)
     # rows, kb, block_rows, source pad before the item, destination gap after it
     mats = [(256, 8, 1, 0, 64), (200, 5, 1, 0, 67), (64, 6, 32, 0, 64), (1408, 64, 32, 0, 61),
-            (128, 12, 1, 1, 64), (384, 16, 1, 3, 64)]
+            (128, 12, 1, 1, 64), (384, 16, 1, 3, 64),
+            # wider than one 160-column work unit: exactly two, and two with a ragged second
+            (256, 320, 1, 0, 64), (200, 200, 1, 0, 64), (96, 176, 32, 0, 64)]
     src_parts, items, refs = [], [], []
     s_off, d_off = 0, 0
     for rows, kb, br, s_pad, gap in mats:
