@@ -77,9 +77,11 @@ def straddling_elems(cfg, plan_info) -> int:
 
 
 # DRAM bytes (read + write) of one Newton-Schulz stage of the Video-DiT x8
-# workload, from profiles/video_dit_launch_list_dram.md, valid for the kernel
-# source it was measured on (sha256 prefix of hm_ns.cu).
-NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.657e+11, "hm_ns_sha256": "bb7a4dd6c3c9d059"}
+# workload with f2 and G folded into its last products (norm, prepare and 30
+# GEMM launches of the timed update), from
+# profiles/video_dit_launch_list_dram.md, valid for the kernel source it was
+# measured on (sha256 prefix of hm_ns.cu).
+NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.787e+11, "hm_ns_sha256": "f4229e266a025f2d"}
 
 
 def ns_stage_traffic(cfg):
@@ -292,13 +294,24 @@ def run_ours(args, cfg):
     info = sess.info
     front = abi.HM_STAGE_F0 | abi.HM_STAGE_GATHER | abi.HM_STAGE_FUSED
     back = abi.HM_STAGE_F2 | abi.HM_STAGE_REQUANT | abi.HM_STAGE_FUSED
+    ns_back = abi.HM_STAGE_STEP & ~(abi.HM_STAGE_F0 | abi.HM_STAGE_GATHER)  # NS, f2 and G; v skipped
 
     def step(ev=None):
-        """One update phase, fused: f0 with the gather folded in, batched
-        Newton-Schulz, then f2 and MXFP8 requant in one pass."""
+        """One update phase, fused: f0 with the gather folded in, then
+        batched Newton-Schulz whose last product applies f2 and the MXFP8
+        requant itself (HM_STAGE_STEP: v never stored)."""
         if ev is None:
-            sess.run(hp, abi.HM_STAGE_ALL_FUSED, stream)
+            sess.run(hp, abi.HM_STAGE_STEP, stream)
             return
+        ev[0].record(stream)
+        sess.run(hp, front, stream)
+        ev[1].record(stream)
+        sess.run(hp, ns_back, stream)
+        ev[2].record(stream)
+
+    def step_through_v(ev):
+        """The same update with v stored by the last product and read back by
+        one f2 + G pass (HM_STAGE_ALL_FUSED, as three calls)."""
         ev[0].record(stream)
         sess.run(hp, front, stream)
         ev[1].record(stream)
@@ -314,7 +327,7 @@ def run_ours(args, cfg):
     if abi.hm_device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -335,10 +348,22 @@ def run_ours(args, cfg):
     clocks.stop()
     ms = t_begin.elapsed_time(t_end)
     stage_ms = {"f0_gather": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
-                "ns": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
-                "f2_requant": statistics.mean(e[2].elapsed_time(e[3]) for e in evs)}
+                "ns_f2_requant": statistics.mean(e[1].elapsed_time(e[2]) for e in evs)}
     if abi.hm_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
+
+    # the same update through v (a separate, shorter timed loop): Newton-Schulz
+    # alone and the f2 + G pass get their own events
+    n_v = min(3, args.steps)
+    vev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_v)]
+    with torch.cuda.stream(stream):
+        for e in vev:
+            step_through_v(e)
+    torch.cuda.synchronize()
+    through_v_ms = {"f0_gather": statistics.mean(e[0].elapsed_time(e[1]) for e in vev),
+                    "ns": statistics.mean(e[1].elapsed_time(e[2]) for e in vev),
+                    "f2_requant": statistics.mean(e[2].elapsed_time(e[3]) for e in vev)}
+    through_v_ms["step"] = sum(through_v_ms.values())
 
     # per-kernel breakdown: the unfused stages, one call each, CUDA events between
     # them (a separate, shorter timed loop after the headline one)
@@ -365,7 +390,7 @@ def run_ours(args, cfg):
     if args.graph:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            sess.run(hp, abi.HM_STAGE_ALL_FUSED, stream)
+            sess.run(hp, abi.HM_STAGE_STEP, stream)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             for _ in range(args.warmup):
@@ -404,9 +429,9 @@ def run_ours(args, cfg):
 
     peaks = load_peaks()
     flops = ns_flops(cfg, cfg.muon.ns_steps)
-    ns_tflops = flops / (stage_ms["ns"] / 1e3) / 1e12
+    ns_tflops = flops / (stage_ms["ns_f2_requant"] / 1e3) / 1e12
     exec_flops = ns_executed_flops(cfg, cfg.muon.ns_steps)
-    exec_tflops = exec_flops / (stage_ms["ns"] / 1e3) / 1e12
+    exec_tflops = exec_flops / (stage_ms["ns_f2_requant"] / 1e3) / 1e12
     P = cfg.numel
     strad = straddling_elems(cfg, info)
     kern = {
@@ -417,14 +442,18 @@ def run_ours(args, cfg):
         "mxfp8_requant": {"gbs": 5.03125 * P / (unfused_ms["requant"] / 1e3) / 1e9, "bytes_per_elem": 5.03125},
         "f0_gather_fused": {"gbs": (14.0 * P + 2.0 * strad) / (stage_ms["f0_gather"] / 1e3) / 1e9,
                             "bytes_per_elem": "14 + 2 per straddling element"},
-        "f2_requant_fused": {"gbs": 13.03125 * P / (stage_ms["f2_requant"] / 1e3) / 1e9,
-                             "bytes_per_elem": 13.03125},
+        "f2_requant_fused": {"gbs": 13.03125 * P / (through_v_ms["f2_requant"] / 1e3) / 1e9,
+                             "bytes_per_elem": 13.03125, "note": "the pass through v (HM_STAGE_ALL_FUSED)"},
     }
     for k in kern:
         if kern[k]["gbs"] is not None:
             kern[k]["frac"] = kern[k]["gbs"] / peaks["hbm_gbs"]
     kern["ns_unfused"] = {"tflops": flops / (unfused_ms["ns"] / 1e3) / 1e12, "ms": unfused_ms["ns"],
                           "frac": flops / (unfused_ms["ns"] / 1e3) / 1e12 / peaks["bf16_sustained"]}
+    kern["ns_through_v"] = {"tflops": flops / (through_v_ms["ns"] / 1e3) / 1e12, "ms": through_v_ms["ns"],
+                            "frac": flops / (through_v_ms["ns"] / 1e3) / 1e12 / peaks["bf16_sustained"],
+                            "executed_frac": exec_flops / (through_v_ms["ns"] / 1e3) / 1e12 /
+                            peaks["bf16_sustained"]}
     if adamw:
         kern["adamw_flat_64M"] = adamw
         adamw["frac"] = adamw["gbs"] / peaks["hbm_gbs"]
@@ -434,7 +463,9 @@ def run_ours(args, cfg):
     roofline = {"bound": "tensor", "achieved": ns_tflops, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                 "frac": ns_tflops / peaks["bf16_sustained"], "traffic": ns_stage_traffic(cfg),
                 "traffic_unit": "DRAM bytes per Newton-Schulz stage (one update), ncu",
-                "kernel": "Newton-Schulz stage: ns_gemm_kernel / ns_gemm_pair_kernel (3 products x 5 iterations per shape class) + norm/prepare",
+                "kernel": "Newton-Schulz stage: ns_gemm_kernel / ns_gemm_pair_kernel (3 products x 5 iterations "
+                          "per shape class) + norm/prepare; the last product also applies f2 and the MXFP8 "
+                          "requant (timed with them)",
                 "peak_kind": f"bf16 dense sustained ({peaks['source']})",
                 "frac_of_burst": ns_tflops / peaks["bf16"],
                 "note": "achieved counts the algorithmic 5(4m^2n+2m^3) FLOP per unit; the kernels skip the "
@@ -459,7 +490,8 @@ def run_ours(args, cfg):
                            "l2": "inputs larger than L2 (resident state ~%.0f GB)" % (
                                (sess.total * 21 + sess.ws_bytes) / 1e9)},
                 "ns_tflops": ns_tflops, "ns_flops_per_step": flops, "ns_executed_flops_per_step": exec_flops,
-                "stages_ms": stage_ms, "unfused_stages_ms": unfused_ms, "kernels": kern,
+                "stages_ms": stage_ms, "through_v_stages_ms": through_v_ms, "unfused_stages_ms": unfused_ms,
+                "kernels": kern,
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
@@ -480,29 +512,33 @@ def e2e_pipelined(sess, hp, stream, steps, dist):
     """Update phases fed from and returned to pinned host memory: every step
     copies its gradient in (9.2 GB for Video-DiT) and its MXFP8 weights and
     scales out.  The copies run on their own streams with double-buffered
-    device gradients, so step k+1's upload and step k's download overlap step
-    k's Newton-Schulz stage; every step's copies are inside the timed
-    region, which runs from the first upload to the last download."""
+    device gradients, MXFP8 weights and scales, so step k+1's upload and step
+    k's download overlap the Newton-Schulz stages; every step's copies are
+    inside the timed region, which runs from the first upload to the last
+    download."""
     import torch
 
     from head_muon_mxfp8_gb300 import abi
     dev = sess.device
     g_dev = [sess.g, torch.empty_like(sess.g)]
     g_dev[1].copy_(sess.g)
+    # q and s double-buffered too: the last products of step k+1 write them
+    # while step k's are still on their way to the host
+    q_dev = [sess.q, torch.empty_like(sess.q)]
+    s_dev = [sess.s, torch.empty_like(sess.s)]
     g_host = torch.empty(sess.total, dtype=torch.float32, pin_memory=True)
     g_host.copy_(sess.g)
     q_host = [torch.empty(sess.total, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
     s_host = [torch.empty(sess.total // 32, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
     bufs = []
-    for g in g_dev:
-        b = abi.hm_muon_bufs(sess.w.data_ptr(), sess.m.data_ptr(), g.data_ptr(), sess.u.data_ptr(),
-                             sess.v.data_ptr(), sess.q.data_ptr(), sess.s.data_ptr())
-        bufs.append(b)
+    for b in range(2):
+        bufs.append(abi.hm_muon_bufs(sess.w.data_ptr(), sess.m.data_ptr(), g_dev[b].data_ptr(), sess.u.data_ptr(),
+                                     sess.v.data_ptr(), q_dev[b].data_ptr(), s_dev[b].data_ptr()))
     cs_in = torch.cuda.Stream(device=dev)
     cs_out = torch.cuda.Stream(device=dev)
     sh = int(stream.cuda_stream)
     front = abi.HM_STAGE_F0 | abi.HM_STAGE_GATHER | abi.HM_STAGE_FUSED
-    back = abi.HM_STAGE_F2 | abi.HM_STAGE_REQUANT | abi.HM_STAGE_FUSED
+    ns_back = abi.HM_STAGE_STEP & ~(abi.HM_STAGE_F0 | abi.HM_STAGE_GATHER)
 
     def run(stages, b):
         abi.muon_update_units(sess.plan, bufs[b], hp, sess.ws, sess.ws_bytes, stages, sh)
@@ -510,7 +546,8 @@ def e2e_pipelined(sess, hp, stream, steps, dist):
     def pipeline(n, t0=None, t1=None):
         ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
         g_free = [None, None]
-        out_done = None
+        out_done = [None, None]
+        last_out = None
         if t0 is not None:
             t0.record(cs_in)
         for k in range(n):
@@ -525,20 +562,19 @@ def e2e_pipelined(sess, hp, stream, steps, dist):
             run(front, b)
             g_free[b] = ev()
             g_free[b].record(stream)
-            run(abi.HM_STAGE_NS, b)
-            if out_done is not None:
-                stream.wait_event(out_done)  # the previous step's download has left q and s
-            run(back, b)
+            if out_done[b] is not None:
+                stream.wait_event(out_done[b])  # step k-2's download has left q[b] and s[b]
+            run(ns_back, b)
             back_done = ev()
             back_done.record(stream)
             with torch.cuda.stream(cs_out):
                 cs_out.wait_event(back_done)
-                q_host[b].copy_(sess.q, non_blocking=True)
-                s_host[b].copy_(sess.s, non_blocking=True)
-                out_done = ev()
-                out_done.record(cs_out)
+                q_host[b].copy_(q_dev[b], non_blocking=True)
+                s_host[b].copy_(s_dev[b], non_blocking=True)
+                out_done[b] = last_out = ev()
+                last_out.record(cs_out)
         if t1 is not None:
-            cs_out.wait_event(out_done)
+            cs_out.wait_event(last_out)
             t1.record(cs_out)
 
     pipeline(1)  # warm-up
@@ -563,7 +599,7 @@ def e2e_pipelined(sess, hp, stream, steps, dist):
     t1 = torch.cuda.Event(enable_timing=True)
     pipeline(steps, t0, t1)
     torch.cuda.synchronize()
-    del g_dev[1]
+    del g_dev[1], q_dev[1], s_dev[1]
     return t0.elapsed_time(t1), rates
 
 

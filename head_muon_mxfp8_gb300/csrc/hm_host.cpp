@@ -23,6 +23,7 @@
 
 using hm::NsClassDev;
 using hm::NsUnit;
+using hm::NsFrag;
 using hm::Range;
 using hm::RangeArgs;
 
@@ -323,6 +324,7 @@ struct UnitPlan {
     int cls = 0;
     int local = 1;
     int64_t stage_off = -1;   // element offset in the u / v staging (straddling units)
+    bool epi = false;         // the last Newton-Schulz product can apply f2 + G itself (kNsEpiUpdate)
     std::vector<hm_fragment> frags;
 };
 
@@ -350,6 +352,13 @@ struct hm_muon_plan {
     std::vector<Range> seg_tab, gather_tab;
     mutable std::vector<Range> f2_tab;
     std::vector<std::pair<int, int>> f2_shape;  // (rows, cols) of each f2 entry's unit
+    // HM_STAGE_SKIP_V: the f2 entries of units the last product cannot update
+    // itself, and every unit's fragments for the ones it can
+    mutable std::vector<Range> f2r_tab;
+    std::vector<std::pair<int, int>> f2r_shape;
+    mutable std::vector<NsUnit> ns_units_dev;  // ns_units with the current steps
+    std::vector<NsFrag> ns_frags;
+    size_t off_f2r = 0, off_nsf = 0;
     // fused update: f0 with the gather folded in (f2 + G reuse the f2 table)
     std::vector<Range> f0x_tab;
     size_t off_f0x = 0;
@@ -395,6 +404,11 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
         q.frags = fragments_of(chain, u.offset, u.offset + ne, 1);
         q.local = q.frags.size() == 1;
         q.exec_rank = q.frags[0].rank;  // owner of the unit's first element
+        // each 1 x 32 MX block a row piece inside one fragment
+        q.epi = u.cols % HM_MX_BLOCK == 0;
+        for (const hm_fragment& f : q.frags)
+            q.epi = q.epi && f.root_offset % HM_MX_BLOCK == 0 && f.unit_offset % HM_MX_BLOCK == 0 &&
+                    f.length % HM_MX_BLOCK == 0;
         if (!q.local) {
             q.stage_off = p->staging_elems;
             p->staging_elems += round_up(ne, 64);
@@ -462,6 +476,12 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
             nu.v_off = nu.u_off;
             nu.flags = (q.local ? 0 : (hm::kNsUStaged | hm::kNsVStaged)) |
                        (u.rows > u.cols ? hm::kNsTransposed : 0);
+            if (q.epi) {
+                nu.flags |= hm::kNsEpiUpdate;
+                nu.frag0 = static_cast<int32_t>(p->ns_frags.size());
+                nu.nfrag = static_cast<int32_t>(q.frags.size());
+                for (const hm_fragment& f : q.frags) p->ns_frags.push_back(NsFrag{f.unit_offset, f.root_offset});
+            }
             p->ns_units.push_back(nu);
         }
         p->classes.push_back(c);
@@ -511,6 +531,18 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
             }
         }
     }
+    pre = 0;
+    for (int i = 0; i < n_units; ++i) {
+        const hm_unit_desc& u = units[i];
+        const UnitPlan& q = p->up[i];
+        if (q.epi) continue;
+        for (const hm_fragment& f : q.frags) {
+            p->f2r_tab.push_back(Range{f.root_offset, q.local ? f.root_offset : q.stage_off + f.unit_offset,
+                                       f.root_offset, f.length, pre, 0.f, q.local ? 0 : 1});
+            p->f2r_shape.push_back({u.rows, u.cols});
+            pre += f.length;
+        }
+    }
 
     // fused-update tables
     pre = 0;
@@ -542,6 +574,8 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
     p->off_gather = take(p->gather_tab.size() * sizeof(Range));
     p->off_f2 = take(p->f2_tab.size() * sizeof(Range));
     p->off_nsu = take(p->ns_units.size() * sizeof(NsUnit));
+    p->off_f2r = take(p->f2r_tab.size() * sizeof(Range));
+    p->off_nsf = take(p->ns_frags.size() * sizeof(NsFrag));
     p->off_f0x = take(p->f0x_tab.size() * sizeof(Range));
     p->off_ustage = take(static_cast<size_t>(p->staging_elems) * 2);
     p->off_vstage = take(static_cast<size_t>(p->staging_elems) * 4);
@@ -646,7 +680,8 @@ extern "C" hm_status muon_plan_upload(hm_muon_plan* p, void* workspace, size_t w
     };
     if (put(p->off_seg, p->seg_tab.data(), p->seg_tab.size() * sizeof(Range)) != cudaSuccess ||
         put(p->off_gather, p->gather_tab.data(), p->gather_tab.size() * sizeof(Range)) != cudaSuccess ||
-        put(p->off_nsu, p->ns_units.data(), p->ns_units.size() * sizeof(NsUnit)) != cudaSuccess)
+        put(p->off_nsu, p->ns_units.data(), p->ns_units.size() * sizeof(NsUnit)) != cudaSuccess ||
+        put(p->off_nsf, p->ns_frags.data(), p->ns_frags.size() * sizeof(NsFrag)) != cudaSuccess)
         return HM_ERR_CUDA;
     for (size_t k = 0; k < p->classes.size(); ++k)
         if (put(p->classes[k].sym_off, p->sym_tab[k].data(), p->sym_tab[k].size() * 4) != cudaSuccess ||
@@ -693,11 +728,20 @@ namespace {
 // re-uploaded, stream-ordered) whenever lr or the alpha mode changes.
 hm_status refresh_steps(const hm_muon_plan* p, const hm_muon_hparams* hp, cudaStream_t s) {
     if (hp->lr == p->f2_lr && hp->alpha_mode == p->f2_alpha_mode) return HM_OK;
-    for (size_t i = 0; i < p->f2_tab.size(); ++i)
-        p->f2_tab[i].step = static_cast<float>(static_cast<double>(hp->lr) *
-                                               alpha_of(hp->alpha_mode, p->f2_shape[i].first, p->f2_shape[i].second));
-    if (!p->f2_tab.empty() && cudaMemcpyAsync(p->ws + p->off_f2, p->f2_tab.data(), p->f2_tab.size() * sizeof(Range),
-                                              cudaMemcpyHostToDevice, s) != cudaSuccess)
+    auto step_of = [&](int rows, int cols) {
+        return static_cast<float>(static_cast<double>(hp->lr) * alpha_of(hp->alpha_mode, rows, cols));
+    };
+    for (size_t i = 0; i < p->f2_tab.size(); ++i) p->f2_tab[i].step = step_of(p->f2_shape[i].first, p->f2_shape[i].second);
+    for (size_t i = 0; i < p->f2r_tab.size(); ++i)
+        p->f2r_tab[i].step = step_of(p->f2r_shape[i].first, p->f2r_shape[i].second);
+    p->ns_units_dev = p->ns_units;
+    for (NsUnit& nu : p->ns_units_dev) nu.step = step_of(nu.rows, nu.cols);
+    auto put = [&](size_t off, const void* src, size_t bytes) {
+        return bytes == 0 || cudaMemcpyAsync(p->ws + off, src, bytes, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    };
+    if (!put(p->off_f2, p->f2_tab.data(), p->f2_tab.size() * sizeof(Range)) ||
+        !put(p->off_f2r, p->f2r_tab.data(), p->f2r_tab.size() * sizeof(Range)) ||
+        !put(p->off_nsu, p->ns_units_dev.data(), p->ns_units_dev.size() * sizeof(NsUnit)))
         return HM_ERR_CUDA;
     p->f2_lr = hp->lr;
     p->f2_alpha_mode = hp->alpha_mode;
@@ -721,8 +765,12 @@ static int64_t device_l2_bytes() {
 
 extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs* b, const hm_muon_hparams* hp,
                                        void* workspace, size_t workspace_bytes, int stages, void* stream) {
-    if (!p || !b || !hp || stages < 0 || stages > (HM_STAGE_ALL | HM_STAGE_FUSED)) return HM_ERR_ARG;
+    if (!p || !b || !hp || stages < 0 || stages > HM_STAGE_STEP) return HM_ERR_ARG;
     const bool fused = stages & HM_STAGE_FUSED;
+    const bool skip_v = stages & HM_STAGE_SKIP_V;
+    // v may stay unwritten only when the same call runs every stage that reads it
+    const int skip_needs = HM_STAGE_NS | HM_STAGE_F2 | HM_STAGE_REQUANT | HM_STAGE_FUSED;
+    if (skip_v && (stages & skip_needs) != skip_needs) return HM_ERR_ARG;
     if (fused) {
         // the fused passes cross stage boundaries: f0 + gather, and f2 + G
         const int front = stages & (HM_STAGE_F0 | HM_STAGE_GATHER);
@@ -828,6 +876,16 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g3.group_m = c.mp / 128;  // column bands: each X panel is fetched once per unit
                 g3.err = g1.err;
                 g3.pace = g1.pace;
+                if (last && skip_v) {
+                    // f2 and G of the kNsEpiUpdate units in this product's epilogue
+                    g3.fuse_update = 1;
+                    g3.decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
+                    g3.has_decay = hp->weight_decay != 0.f;
+                    g3.frags = reinterpret_cast<const NsFrag*>(ws + p->off_nsf);
+                    g3.w = b->w;
+                    g3.q = b->q;
+                    g3.s = b->s;
+                }
                 if (pair) {
                     // B X raster for pairs: tile columns within bands of tile-rows, the
                     // fewest equal bands whose slab of B fits in a quarter of the L2 --
@@ -848,9 +906,11 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
         }
     }
     if (fused && (stages & HM_STAGE_F2)) {
-        // f2 and G in one pass: the new w of every element is quantized as it is written
-        if (!p->f2_tab.empty()) {
-            RangeArgs ra = device_ranges(ws, p->off_f2, p->f2_tab);
+        // f2 and G in one pass: the new w of every element is quantized as it is
+        // written (with HM_STAGE_SKIP_V only for units the last product left)
+        const std::vector<Range>& tab = skip_v ? p->f2r_tab : p->f2_tab;
+        if (!tab.empty()) {
+            RangeArgs ra = device_ranges(ws, skip_v ? p->off_f2r : p->off_f2, tab);
             const float decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
             if (hm::launch_f2_requant(ra, b->w, b->v, v_stage, b->q, b->s, decay, hp->weight_decay != 0.f, s) !=
                 cudaSuccess)

@@ -48,12 +48,25 @@ struct NsUnit {
     int32_t rows;    // unit as stored: rows x cols, row-major
     int32_t cols;
     int32_t flags;   // kNs* bits
-    int32_t pad;
+    float   step;    // kNsEpiUpdate: fp32(lr * alpha), as in the f2 table
+    int32_t frag0;   // kNsEpiUpdate: first of the unit's nfrag entries in the fragment table
+    int32_t nfrag;
 };
-static_assert(sizeof(NsUnit) == 32, "NsUnit layout");
+static_assert(sizeof(NsUnit) == 40, "NsUnit layout");
 constexpr int kNsUStaged = 1;       // u read from staging
 constexpr int kNsVStaged = 2;       // v written to staging
 constexpr int kNsTransposed = 4;    // rows > cols: X = u^T
+constexpr int kNsEpiUpdate = 8;     // the last product may apply f2 and G itself: cols and
+                                    // every fragment a multiple of 32, so each 1 x 32 MX
+                                    // block is one row piece of the unit in one fragment
+
+// Where a unit's elements live in the roots of w, q (element offsets) and s
+// (offset / 32): unit elements [unit_off, next entry's unit_off) start at
+// root_off.  A unit's entries are in unit order; a local unit has one.
+struct NsFrag {
+    int64_t unit_off;
+    int64_t root_off;
+};
 
 // A Newton-Schulz shape class: units with the same (m, n) = (min, max) of
 // (rows, cols).  X is stored padded to mp x np (mp multiple of 128, np
@@ -99,6 +112,15 @@ struct GemmParams {
     int32_t inject_no_ready;  // failure test: never signal an accumulator as ready
     int32_t* pace;            // CTA-pair kernel: 2 device ints (tiles issued, pairs done), zero between
                               // launches; nullptr = pairs run unpaced
+    // final product with the update folded in (units flagged kNsEpiUpdate):
+    // w <- w*decay - step*v and G on the new w, v itself never stored
+    int32_t fuse_update;
+    int32_t has_decay;
+    float decay;
+    const NsFrag* frags;
+    float* w;
+    uint8_t* q;
+    uint8_t* s;
 };
 
 // chain geometry the device needs: z1 edges and the segment base of every chunk

@@ -8,7 +8,8 @@
 //   repeat: A = X X^T;  B = b A + c A A;  X = a X + B X;
 //   v = X (transposed back).
 // A, B and X are rounded to bf16 after each product (fp32 accumulation in
-// TMEM); the last product is written to v in fp32.
+// TMEM); the last product is written to v in fp32 or, when the caller folds
+// f2 and G into it, applied to w and quantized to (q, s) without storing v.
 //
 // Layout in the workspace, per shape class of U units:
 //   X[2]   bf16 [U][mp][np]   (ping-pong)
@@ -34,6 +35,7 @@
 // records HM_ERR_TIMEOUT in the device error word, lets every role finish,
 // waits for its own TMA copies and MMAs, frees TMEM and returns.
 #include "hm_internal.h"
+#include "hm_mx_device.cuh"
 
 #include <cuda_bf16.h>
 
@@ -391,6 +393,120 @@ __device__ __forceinline__ void load_addend_chunk(const GemmParams& p, int u, in
         a[s] = __ldg(reinterpret_cast<const uint4*>(ab + static_cast<int64_t>(i0 + (lane >> 2) + 8 * s) * p.ld_add));
 }
 
+// The fragment of a kNsEpiUpdate unit that holds unit element e (a block start).
+__device__ __forceinline__ int64_t unit_root_offset(const GemmParams& p, const NsUnit& nu, int64_t e) {
+    int f = nu.frag0;
+    while (f + 1 < nu.frag0 + nu.nfrag && p.frags[f + 1].unit_off <= e) ++f;
+    return p.frags[f].root_off + (e - p.frags[f].unit_off);
+}
+
+// 16-byte chunk c4 of row r of a warp's 32 x 32 fp32 staging tile: chunk c4
+// of row r sits at c4 ^ (r % 8), so row-wise writes and 4-lanes-per-row reads
+// are both conflict-free.
+__device__ __forceinline__ float4* stage4(float* stage, int r, int c4) {
+    return reinterpret_cast<float4*>(stage + r * 32 + ((c4 ^ (r & 7)) << 2));
+}
+
+// staging += beta * addend (the aX term of the last product), in the layout
+// of load_addend_chunk: lane l holds row l/4 + 8s, columns 8(l%4)..+7.
+__device__ __forceinline__ void stage_add_addend(const GemmParams& p, float* stage, const uint4 (&a)[4]) {
+    const int lane = threadIdx.x & 31;
+    const int cq = (lane & 3) * 8;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int rr = (lane >> 2) + 8 * s;
+        float a8[8];
+        unpack_bf16x8(a[s], a8);
+        float4* p0 = stage4(stage, rr, cq >> 2);
+        float4* p1 = stage4(stage, rr, (cq >> 2) + 1);
+        const float4 y0 = *p0, y1 = *p1;
+        *p0 = make_float4(fmaf(p.beta, a8[0], y0.x), fmaf(p.beta, a8[1], y0.y), fmaf(p.beta, a8[2], y0.z),
+                          fmaf(p.beta, a8[3], y0.w));
+        *p1 = make_float4(fmaf(p.beta, a8[4], y1.x), fmaf(p.beta, a8[5], y1.y), fmaf(p.beta, a8[6], y1.z),
+                          fmaf(p.beta, a8[7], y1.w));
+    }
+}
+
+// Last product with the update folded in (units flagged kNsEpiUpdate): the
+// chunk's 32 x 32 values of v = aX + BX (fp32, in the warp's swizzled staging
+// tile) never reach memory.  Each 1 x 32 MX block of the unit's w that the
+// chunk covers -- a row of the chunk, or a column when the unit is stored
+// transposed (X = u^T) -- is read from the root, updated as f2 does it
+// (w*decay - step*v, or w - step*v, each product and the difference rounded
+// once) and quantized as G does it, so w, q and s come out bit-identical to
+// the pass through v.  Four lanes own one block, 8 elements each (lane l:
+// block l/4 + 8s, elements 8(l%4)..+7); the loads of all four blocks go first.
+// (Issuing them before the aX addend is folded in, or a tile ahead as L2
+// prefetches, measured no faster.)
+//
+// base1: root offset minus unit offset of a unit with one fragment (a local
+// unit), read once per tile; -1 = look the fragment up per block.
+__device__ __forceinline__ void final_update_chunk(const GemmParams& p, const NsUnit& nu, int64_t base1,
+                                                   const float* stage, int i0, int j0) {
+    const int lane = threadIdx.x & 31;
+    const bool tr = nu.flags & kNsTransposed;
+    const int kw = tr ? p.m_real : p.n_real;      // length of a row of w (the MX K)
+    const int rows_w = tr ? p.n_real : p.m_real;  // rows of w
+    const int rw0 = tr ? j0 : i0;                  // w row of the chunk's block 0
+    const int cw0 = tr ? i0 : j0;                  // w column of every block's first element
+    if (cw0 >= kw) return;                         // padding of X (warp-uniform)
+    const int cq = (lane & 3) * 8;
+    int64_t dst[4];
+    float4 w0[4], w1[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int rw = rw0 + (lane >> 2) + 8 * s;
+        w0[s] = w1[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dst[s] = -1;
+        if (rw >= rows_w) continue;
+        // the unit's fragment that holds this block (32-aligned: the whole block)
+        const int64_t e = static_cast<int64_t>(rw) * kw + cw0;
+        dst[s] = base1 >= 0 ? base1 + e : unit_root_offset(p, nu, e);
+        const float4* wp = reinterpret_cast<const float4*>(p.w + dst[s] + cq);
+        w0[s] = __ldcs(wp);
+        w1[s] = __ldcs(wp + 1);
+    }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int kk = (lane >> 2) + 8 * s;
+        float y[8];
+        if (tr) {
+            // column kk of the chunk, rows cq..cq+7 (chunk c of row r sits at c ^ (r % 8))
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = stage[(cq + e) * 32 + ((((kk >> 2) ^ e) << 2) | (kk & 3))];
+        } else {
+            const float4 a = *reinterpret_cast<const float4*>(stage + kk * 32 + (((cq >> 2) ^ (kk & 7)) << 2));
+            const float4 b = *reinterpret_cast<const float4*>(stage + kk * 32 + ((((cq >> 2) + 1) ^ (kk & 7)) << 2));
+            y[0] = a.x; y[1] = a.y; y[2] = a.z; y[3] = a.w;
+            y[4] = b.x; y[5] = b.y; y[6] = b.z; y[7] = b.w;
+        }
+        const float wv[8] = {w0[s].x, w0[s].y, w0[s].z, w0[s].w, w1[s].x, w1[s].y, w1[s].z, w1[s].w};
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float a = p.has_decay ? __fmul_rn(wv[e], p.decay) : wv[e];
+            x[e] = __fsub_rn(a, __fmul_rn(nu.step, y[e]));
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        if (dst[s] < 0) continue;  // a row of w beyond the unit (same for the block's 4 lanes)
+        float4* wp = reinterpret_cast<float4*>(p.w + dst[s] + cq);
+        __stcs(wp, make_float4(x[0], x[1], x[2], x[3]));
+        __stcs(wp + 1, make_float4(x[4], x[5], x[6], x[7]));
+        const int ex = mx_scale_exponent(amax);
+        const float sc = mx_inv_scale(ex);
+        const uint32_t c01 = cvt_e4m3x2(x[0] * sc, x[1] * sc);
+        const uint32_t c23 = cvt_e4m3x2(x[2] * sc, x[3] * sc);
+        const uint32_t c45 = cvt_e4m3x2(x[4] * sc, x[5] * sc);
+        const uint32_t c67 = cvt_e4m3x2(x[6] * sc, x[7] * sc);
+        __stcs(reinterpret_cast<uint2*>(p.q + dst[s] + cq), make_uint2(c01 | (c23 << 16), c45 | (c67 << 16)));
+        if ((lane & 3) == 0) p.s[dst[s] >> 5] = static_cast<uint8_t>(ex + 127);
+    }
+}
+
 // i_base: first output row of this CTA's 128-row slab of the tile.  `next`
 // holds the addend of the warp's first chunk when addend_coalesced(p): the
 // caller loads it before waiting for the accumulator, and each chunk loads
@@ -400,6 +516,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                                               float* stage, int half, uint4 (&next)[4]) {
     const int i = i_base + row;
     const int c_end = (half + 1) * (BN / 64);
+    // last product: the unit's destination once per tile
+    NsUnit nu{};
+    bool fuse = false;
+    int64_t base1 = -1;
+    if (p.epi == kEpiFinal) {
+        nu = p.ns_units[u];
+        fuse = p.fuse_update && (nu.flags & kNsEpiUpdate);
+        if (fuse && nu.nfrag == 1) base1 = p.frags[nu.frag0].root_off - p.frags[nu.frag0].unit_off;
+    }
     // the next chunk's TMEM load is in flight while the current chunk is processed
     uint32_t rn[32];
     __syncwarp();
@@ -452,22 +577,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                 }
                 continue;
             }
-            // last iteration: v = fp32(aX + BX) into the unit's own v location
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const int rr = (lane >> 2) + 8 * s;
-                float a8[8];
-                unpack_bf16x8(a[s], a8);
-                float4* p0 = st4(rr, cq >> 2);
-                float4* p1 = st4(rr, (cq >> 2) + 1);
-                const float4 y0 = *p0, y1 = *p1;
-                *p0 = make_float4(fmaf(p.beta, a8[0], y0.x), fmaf(p.beta, a8[1], y0.y), fmaf(p.beta, a8[2], y0.z),
-                                  fmaf(p.beta, a8[3], y0.w));
-                *p1 = make_float4(fmaf(p.beta, a8[4], y1.x), fmaf(p.beta, a8[5], y1.y), fmaf(p.beta, a8[6], y1.z),
-                                  fmaf(p.beta, a8[7], y1.w));
-            }
+            // last iteration: v = fp32(aX + BX) into the unit's own v location,
+            // or f2 and G of the unit straight from the staging
+            stage_add_addend(p, stage, a);
             __syncwarp();
-            const NsUnit nu = p.ns_units[u];
+            if (fuse) {
+                final_update_chunk(p, nu, base1, stage, i0, j0);
+                __syncwarp();
+                continue;
+            }
             float* dst = ((nu.flags & kNsVStaged) ? p.v_stage : p.v_root) + nu.v_off;
             if (nu.flags & kNsTransposed) {
                 // v is X^T: for each k the 32 lanes write 32 consecutive floats

@@ -39,17 +39,24 @@ def _sample_units(cfg, s, hm, rng):
 
 @pytest.mark.parametrize("name", ["lm_layer", "moe_layer", "video_dit"])
 def test_fullsize_update_sampled(hm, dev, name):
+    """The benchmark's stage set (HM_STAGE_STEP: f2 and G in the last
+    product's epilogue, no v) against the same update through v
+    (HM_STAGE_ALL_FUSED) on a second session: m, u, w, q, s equal bit for
+    bit over the whole tensor list; v of the second session then carries the
+    Newton-Schulz and f2 checks."""
     from head_muon_mxfp8_gb300.session import MuonSession, muon_hparams
     cfg = workloads.get(name)
     rng = np.random.default_rng(7)
     s = MuonSession.from_config(cfg, device=dev)
+    s_v = MuonSession.from_config(cfg, device=dev)
     data = workloads.generate_device(cfg, dev, seed=3)
     gen = torch.Generator(device=dev)
     gen.manual_seed(5)
     m0 = torch.empty(cfg.numel, dtype=torch.float32, device=dev).normal_(0.0, 1e-3, generator=gen)
-    s.load("w", data["w"])
-    s.load("g", data["g"])
-    s.load("m", m0)
+    for x in (s, s_v):
+        x.load("w", data["w"])
+        x.load("g", data["g"])
+        x.load("m", m0)
     # the samples the oracle will need, taken before the update
     idx = torch.from_numpy(np.sort(rng.choice(cfg.numel, 1 << 20, replace=False))).to(dev)
     w0_s, g_s, m0_s = data["w"][idx].cpu().numpy(), data["g"][idx].cpu().numpy(), m0[idx].cpu().numpy()
@@ -57,9 +64,15 @@ def test_fullsize_update_sampled(hm, dev, name):
     w0_units = {i: data["w"][cfg.units[i].offset:cfg.units[i].offset + cfg.units[i].numel].cpu().numpy()
                 for i in units}
     del data, m0
-    s.run(muon_hparams(cfg.muon))
+    s.run(muon_hparams(cfg.muon), hm.HM_STAGE_STEP)
+    s_v.run(muon_hparams(cfg.muon), hm.HM_STAGE_ALL_FUSED)
     torch.cuda.synchronize()
     assert hm.hm_device_error() == 0
+    for f in ("m", "u", "w", "q", "s"):
+        a, b = getattr(s, f), getattr(s_v, f)
+        if a.dtype == torch.float32:  # bit patterns: the guard words between segments are NaNs
+            a, b = a.view(torch.int32), b.view(torch.int32)
+        assert torch.equal(a, b), f"{f}: HM_STAGE_STEP differs from the pass through v"
     # f0 on sampled elements (bit-exact)
     m_ref, u_ref = OM.momentum(m0_s, g_s, cfg.muon.momentum)
     m_all = s.fetch("m")
@@ -73,13 +86,15 @@ def test_fullsize_update_sampled(hm, dev, name):
         u_bits = u_all[un.offset:un.offset + un.numel].numpy().view(np.uint16)
         ref = OM.newton_schulz(OM.bf16_bits_to_f32(u_bits).reshape(un.rows, un.cols), h.ns_steps, h.ns_a, h.ns_b,
                                h.ns_c, h.eps)
-        v = s.unit_v(i).numpy()
+        v = s_v.unit_v(i).numpy()
         err = np.linalg.norm(v.astype(np.float64) - ref.ravel()) / np.linalg.norm(ref)
         assert err <= NS_TOL, f"unit {i} {un.rows}x{un.cols}: {err:.3e}"
         w1 = s.fetch_range("w", un.offset, un.offset + un.numel).numpy()
         want = OM.main_weight_update(w0_units[i], v, h.lr, 1.0)
         assert np.array_equal(w1.view(np.uint32), want.view(np.uint32))
     del m_all, u_all
+    assert all(s_v.canary_intact().values())
+    s_v.close()
     # MXFP8 on sampled blocks (bit-exact on the device's updated w)
     w_all = s.fetch("w").numpy()
     q_all = s.fetch("q").numpy()

@@ -27,9 +27,10 @@ def _state(s):
     return {f: s.fetch(f).numpy().copy() for f in ("w", "m", "q", "s")}
 
 
-@pytest.mark.parametrize("name", ["tiny", "mixed"])
-def test_fused_update_replayed_from_a_cuda_graph_equals_eager(hm, dev, name):
+@pytest.mark.parametrize("name,step", [("tiny", False), ("mixed", False), ("tiny", True), ("mixed", True)])
+def test_fused_update_replayed_from_a_cuda_graph_equals_eager(hm, dev, name, step):
     from head_muon_mxfp8_gb300.session import MuonSession, muon_hparams
+    stages = hm.HM_STAGE_STEP if step else hm.HM_STAGE_ALL_FUSED
     cfg = workloads.get(name)
     data = workloads.generate(cfg, seed=17)
     hp = muon_hparams(cfg.muon)
@@ -39,7 +40,7 @@ def test_fused_update_replayed_from_a_cuda_graph_equals_eager(hm, dev, name):
     eager.load("g", data["g"])
     eager.load("m", np.zeros_like(data["w"]))
     for _ in range(2):
-        eager.run(hp, hm.HM_STAGE_ALL_FUSED)
+        eager.run(hp, stages)
     torch.cuda.synchronize()
     want = _state(eager)
     eager.close()
@@ -49,7 +50,7 @@ def test_fused_update_replayed_from_a_cuda_graph_equals_eager(hm, dev, name):
     # one eager call on the capture stream first: first-use setup (kernel
     # attributes, the f2 step table) happens outside the capture
     s.load("m", np.zeros_like(data["w"]))
-    s.run(hp, hm.HM_STAGE_ALL_FUSED, side)
+    s.run(hp, stages, side)
     torch.cuda.synchronize()
     s.load("w", data["w"])
     s.load("g", data["g"])
@@ -58,7 +59,7 @@ def test_fused_update_replayed_from_a_cuda_graph_equals_eager(hm, dev, name):
     graph = torch.cuda.CUDAGraph()
     before = hm.hm_kernel_launches()
     with torch.cuda.graph(graph, stream=side):
-        s.run(hp, hm.HM_STAGE_ALL_FUSED, side)
+        s.run(hp, stages, side)
     captured = hm.hm_kernel_launches() - before
     assert captured > 0
     torch.cuda.synchronize()

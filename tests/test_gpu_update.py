@@ -134,15 +134,33 @@ def _logical_v(hm, s, cfg):
     return v
 
 
+def _epilogue_updated(cfg, i):
+    """Units whose last Newton-Schulz product applies f2 and G itself under
+    HM_STAGE_SKIP_V: every MX block a piece of one row (cols a multiple of 32;
+    the test chains' fragments are 32-aligned)."""
+    return cfg.units[i].cols % 32 == 0
+
+
+V_UNTOUCHED = np.uint32(0x7FC0ABCD)  # a NaN payload no update produces
+
+
 @pytest.mark.parametrize("name,variant", [("tiny", "plain"), ("tiny_ragged", "plain"), ("mixed", "plain"),
-                                          ("mixed", "decay_alpha"), ("moe_small", "plain")])
+                                          ("mixed", "decay_alpha"), ("moe_small", "plain"),
+                                          ("ragged_n", "decay_alpha")])
 def test_fused_update_equals_unfused(hm, dev, name, variant):
     """HM_STAGE_ALL_FUSED (gather folded into f0; f2 and G in one pass) gives
     bit-identical m, u, v, w, q, s to the unfused stages, over two
-    consecutive updates; its w is f2 of the unfused v."""
+    consecutive updates; its w is f2 of the unfused v.  HM_STAGE_STEP (f2
+    and G in the last product's epilogue, v skipped) gives the same m, u, w,
+    q, s bit for bit, writes v only for the units it cannot update in the
+    epilogue (cols not a multiple of 32) and leaves the others' v as it was."""
     if name == "moe_small":
         cfg = workloads.scaled_muon("moe_small", [(256, 384, None)] * 6 + [(384, 256, None)] * 3, so=8, sw=4, sg=4)
         cfg.edge_shift = workloads.ragged_shift(8, 300, seed=5)
+    elif name == "ragged_n":
+        # transposed (100 x 64) and ragged (cols 100, 72, 80) units side by side
+        cfg = workloads.scaled_muon("ragged_n", [(64, 100, None), (100, 64, None), (32, 72, None), (48, 80, None),
+                                                 (160, 64, None), (64, 160, None)], so=4, sw=2, sg=2)
     else:
         cfg = workloads.get(name)
     if variant == "decay_alpha":
@@ -150,33 +168,55 @@ def test_fused_update_equals_unfused(hm, dev, name, variant):
     data = workloads.generate(cfg, seed=17)
     grads = [data["g"], workloads.gaussian(cfg.numel, cfg.g_std, seed=19)]
     m0 = workloads.gaussian(cfg.numel, 1e-3, seed=18)
+    v_mark = np.full(cfg.numel, V_UNTOUCHED, dtype=np.uint32).view(np.float32)
     results = {}
-    for stages in (hm.HM_STAGE_ALL, hm.HM_STAGE_ALL_FUSED):
+    for stages in (hm.HM_STAGE_ALL, hm.HM_STAGE_ALL_FUSED, hm.HM_STAGE_STEP):
         s = _session(cfg, dev)
         s.load("w", data["w"])
         s.load("m", m0)
         per_step = []
         for g in grads:
             s.load("g", g)
+            s.load("v", v_mark)
             s.run(_hp(cfg.muon), stages)
             torch.cuda.synchronize()
             out = {k: s.fetch(k).numpy() for k in ("m", "u", "w", "q", "s")}
             out["v"] = _logical_v(hm, s, cfg)
+            out["v_root"] = s.fetch("v").numpy()
             per_step.append(out)
         assert all(s.canary_intact().values())
         assert hm.hm_device_error() == 0
         results[stages] = per_step
+        epi = [_epilogue_updated(cfg, i) for i in range(len(cfg.units))]
+        local = [hm.muon_plan_unit(s.plan, i)["local"] for i in range(len(cfg.units))]
         s.close()
     w_prev = data["w"]
-    for ref, got in zip(results[hm.HM_STAGE_ALL], results[hm.HM_STAGE_ALL_FUSED]):
+    for ref, got, step in zip(results[hm.HM_STAGE_ALL], results[hm.HM_STAGE_ALL_FUSED], results[hm.HM_STAGE_STEP]):
         for k in ("m", "u", "v", "w", "q", "s"):
             a, b = ref[k], got[k]
             if a.dtype == np.float32:
                 a, b = a.view(np.uint32), b.view(np.uint32)
             assert np.array_equal(a, b), f"fused {k} differs"
+        for k in ("m", "u", "w", "q", "s"):
+            a, b = ref[k], step[k]
+            if a.dtype == np.float32:
+                a, b = a.view(np.uint32), b.view(np.uint32)
+            assert np.array_equal(a, b), f"HM_STAGE_STEP {k} differs"
+        for i, un in enumerate(cfg.units):
+            sl = slice(un.offset, un.offset + un.numel)
+            if not epi[i]:
+                assert np.array_equal(step["v"][sl].view(np.uint32), ref["v"][sl].view(np.uint32)), f"unit {i} v"
+            elif local[i]:
+                assert (step["v_root"][sl].view(np.uint32) == V_UNTOUCHED).all(), f"unit {i} v written"
         check_f2(cfg, w_prev, ref["v"], got["w"], cfg.muon)
-        check_requant(cfg, got["w"], got["q"], got["s"])
+        if name == "ragged_n":
+            # K not a multiple of 32: G takes the flat 32-element groups of the segments
+            q_ref, s_ref = OX.requant_list(got["w"], [(0, cfg.numel // 32, 32)])
+            assert np.array_equal(got["q"], q_ref) and np.array_equal(got["s"], s_ref)
+        else:
+            check_requant(cfg, got["w"], got["q"], got["s"])
         w_prev = got["w"]
+    assert any(epi) and (name != "ragged_n" or not all(epi))
 
 
 def test_fused_stage_sets_are_validated(hm, dev):
@@ -185,7 +225,11 @@ def test_fused_stage_sets_are_validated(hm, dev):
     s = _session(cfg, dev)
     hp = _hp(cfg.muon)
     for bad in (hm.HM_STAGE_F0 | hm.HM_STAGE_FUSED, hm.HM_STAGE_GATHER | hm.HM_STAGE_FUSED,
-                hm.HM_STAGE_NS | hm.HM_STAGE_F2 | hm.HM_STAGE_FUSED, hm.HM_STAGE_REQUANT | hm.HM_STAGE_FUSED):
+                hm.HM_STAGE_NS | hm.HM_STAGE_F2 | hm.HM_STAGE_FUSED, hm.HM_STAGE_REQUANT | hm.HM_STAGE_FUSED,
+                # v may be skipped only when the same call consumes it
+                hm.HM_STAGE_ALL | hm.HM_STAGE_SKIP_V, hm.HM_STAGE_NS | hm.HM_STAGE_SKIP_V,
+                hm.HM_STAGE_NS | hm.HM_STAGE_F2 | hm.HM_STAGE_REQUANT | hm.HM_STAGE_SKIP_V,
+                hm.HM_STAGE_STEP + 1):
         st = hm.lib().muon_update_units(C.c_void_p(s.plan), C.byref(s.bufs), C.byref(hp), C.c_void_p(s.ws),
                                         s.ws_bytes, bad, None)
         assert st == hm.HM_ERR_ARG
@@ -297,12 +341,13 @@ def test_empty_inputs_are_noops(hm, dev):
     assert hm.hm_device_error() == 0
 
 
-@pytest.mark.parametrize("name", ["tiny", "mixed"])
-def test_kernel_launch_count_of_one_fused_update(hm, dev, name):
+@pytest.mark.parametrize("name,step", [("tiny", False), ("mixed", False), ("tiny", True), ("mixed", True)])
+def test_kernel_launch_count_of_one_fused_update(hm, dev, name, step):
     """One fused update launches f0 (with the gather), per shape class the
     norm partials, the norm total, the prepare pass and 3 products per
-    Newton-Schulz iteration, then f2 with the requant: the library's launch
-    counter reports exactly that many kernels."""
+    Newton-Schulz iteration, then f2 with the requant -- which HM_STAGE_STEP
+    drops when the last products update every unit themselves: the
+    library's launch counter reports exactly that many kernels."""
     cfg = workloads.get(name)
     data = workloads.generate(cfg, seed=5)
     s = _session(cfg, dev)
@@ -310,10 +355,12 @@ def test_kernel_launch_count_of_one_fused_update(hm, dev, name):
     s.load("g", data["g"])
     hp = _hp(cfg.muon)
     before = hm.hm_kernel_launches()
-    s.run(hp, hm.HM_STAGE_ALL_FUSED)
+    s.run(hp, hm.HM_STAGE_STEP if step else hm.HM_STAGE_ALL_FUSED)
     n = hm.hm_kernel_launches() - before
     torch.cuda.synchronize()
-    assert n == 2 + s.info.n_classes * (3 + 3 * cfg.muon.ns_steps)
+    assert hm.hm_device_error() == 0
+    rest = not step or not all(_epilogue_updated(cfg, i) for i in range(len(cfg.units)))
+    assert n == 1 + s.info.n_classes * (3 + 3 * cfg.muon.ns_steps) + int(rest)
 
 
 def test_newton_schulz_ragged_row_tails(hm, dev):
