@@ -81,7 +81,7 @@ def straddling_elems(cfg, plan_info) -> int:
 # GEMM launches of the timed update), from
 # profiles/video_dit_launch_list_dram.md, valid for the kernel source it was
 # measured on (sha256 prefix of hm_ns.cu).
-NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.787e+11, "hm_ns_sha256": "f4229e266a025f2d"}
+NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.799e+11, "hm_ns_sha256": "6fab17f40d136d39"}
 
 
 def ns_stage_traffic(cfg):

@@ -369,6 +369,11 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& x, float* f) {
     }
 }
 __device__ __forceinline__ uint32_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+// Two floats rounded to bf16 (RNE) in one conversion; lo in the low half.
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
 
 // Epilogues that add aX read the addend with 4 lanes per row (see below).
 __device__ __forceinline__ bool addend_coalesced(const GemmParams& p) {
@@ -572,8 +577,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
 #pragma unroll
                     for (int t = 0; t < 8; ++t) o[t] = fmaf(p.beta, a8[t], y[t]);
                     *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(i0 + rr) * p.ld_out) = make_uint4(
-                        bf16_bits(o[0]) | (bf16_bits(o[1]) << 16), bf16_bits(o[2]) | (bf16_bits(o[3]) << 16),
-                        bf16_bits(o[4]) | (bf16_bits(o[5]) << 16), bf16_bits(o[6]) | (bf16_bits(o[7]) << 16));
+                        bf16x2_bits(o[0], o[1]), bf16x2_bits(o[2], o[3]),
+                        bf16x2_bits(o[4], o[5]), bf16x2_bits(o[6], o[7]));
                 }
                 continue;
             }
@@ -678,8 +683,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                     const int rr = (lane >> 2) + 8 * s;
                     const float4 y0 = *st4(rr, cq >> 2), y1 = *st4(rr, (cq >> 2) + 1);
                     *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(i0 + rr) * p.ld_out + j0 + cq) = make_uint4(
-                        bf16_bits(y0.x) | (bf16_bits(y0.y) << 16), bf16_bits(y0.z) | (bf16_bits(y0.w) << 16),
-                        bf16_bits(y1.x) | (bf16_bits(y1.y) << 16), bf16_bits(y1.z) | (bf16_bits(y1.w) << 16));
+                        bf16x2_bits(y0.x, y0.y), bf16x2_bits(y0.z, y0.w),
+                        bf16x2_bits(y1.x, y1.y), bf16x2_bits(y1.z, y1.w));
                 }
                 // mirror: row j0 + kk of the output takes column kk of the chunk,
                 // 8 of its rows per lane
@@ -691,8 +696,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                     for (int e = 0; e < 8; ++e)
                         y[e] = stage[(cq + e) * 32 + ((((kk >> 2) ^ e) << 2) | (kk & 3))];
                     *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(j0 + kk) * p.ld_out + i0 + cq) = make_uint4(
-                        bf16_bits(y[0]) | (bf16_bits(y[1]) << 16), bf16_bits(y[2]) | (bf16_bits(y[3]) << 16),
-                        bf16_bits(y[4]) | (bf16_bits(y[5]) << 16), bf16_bits(y[6]) | (bf16_bits(y[7]) << 16));
+                        bf16x2_bits(y[0], y[1]), bf16x2_bits(y[2], y[3]),
+                        bf16x2_bits(y[4], y[5]), bf16x2_bits(y[6], y[7]));
                 }
             }
             __syncwarp();
@@ -715,10 +720,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
         uint4 pk[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            pk[q] = make_uint4(bf16_bits(v[8 * q + 0]) | (bf16_bits(v[8 * q + 1]) << 16),
-                               bf16_bits(v[8 * q + 2]) | (bf16_bits(v[8 * q + 3]) << 16),
-                               bf16_bits(v[8 * q + 4]) | (bf16_bits(v[8 * q + 5]) << 16),
-                               bf16_bits(v[8 * q + 6]) | (bf16_bits(v[8 * q + 7]) << 16));
+            pk[q] = make_uint4(bf16x2_bits(v[8 * q + 0], v[8 * q + 1]),
+                               bf16x2_bits(v[8 * q + 2], v[8 * q + 3]),
+                               bf16x2_bits(v[8 * q + 4], v[8 * q + 5]),
+                               bf16x2_bits(v[8 * q + 6], v[8 * q + 7]));
         uint4* op = reinterpret_cast<uint4*>(p.out + u * p.out_us + static_cast<int64_t>(i) * p.ld_out + j0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) op[q] = pk[q];
