@@ -41,7 +41,7 @@ HM_STAGE_REQUANT = 16
 HM_STAGE_ALL = 31
 HM_STAGE_FUSED = 32
 HM_STAGE_ALL_FUSED = 63
-HM_STAGE_SKIP_V = 64
+HM_STAGE_SCRATCH = 64
 HM_STAGE_STEP = 127
 HM_RS_FP32, HM_RS_BF16, HM_RS_BF16_SR = 0, 1, 2
 

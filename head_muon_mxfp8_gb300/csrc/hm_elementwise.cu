@@ -56,11 +56,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // ---------------------------------------------------------------------------
 // f0: m <- mu*m + g (fp32, multiply then add, each rounded); u = bf16_RNE(m)
 // (Nesterov: u = bf16_RNE(g + mu*m_new)).  8 elements per thread step.
+// stage_only: fragments of straddling units write u to their staging only.
 // ---------------------------------------------------------------------------
 template <int V>
 __global__ void __launch_bounds__(kThreads) f0_kernel(const __grid_constant__ RangeArgs ra, float* __restrict__ m,
                                                        const float* __restrict__ g, uint16_t* __restrict__ u,
-                                                       uint16_t* __restrict__ u_stage, float mu, int nesterov) {
+                                                       uint16_t* __restrict__ u_stage, float mu, int nesterov,
+                                                       int stage_only) {
     // V vectors of 8 elements per thread and step: all their loads are issued
     // before the first one is used
     for (int64_t t0 = blockIdx.x * kTile; t0 < ra.total; t0 += static_cast<int64_t>(gridDim.x) * kTile) {
@@ -101,9 +103,9 @@ __global__ void __launch_bounds__(kThreads) f0_kernel(const __grid_constant__ Ra
                 __stcs(mp + 1, make_float4(mv[4], mv[5], mv[6], mv[7]));
                 uint4 pk = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]),
                                       pack_bf16x2(src[4], src[5]), pack_bf16x2(src[6], src[7]));
-                *reinterpret_cast<uint4*>(u + e[q]) = pk;
-                // fused gather: a fragment of a straddling unit also lands in its staging
+                // fused gather: a fragment of a straddling unit also (or only) lands in its staging
                 const Range& r = range_at(ra, rv[q]);
+                if (!(stage_only && (r.flags & 2))) *reinterpret_cast<uint4*>(u + e[q]) = pk;
                 if (r.flags & 2) *reinterpret_cast<uint4*>(u_stage + r.b + d[q]) = pk;
             }
         }
@@ -487,11 +489,11 @@ int32_t* device_error_word() {
 }
 
 cudaError_t launch_f0(const RangeArgs& ra, float* m, const float* g, uint16_t* u, uint16_t* u_stage, float mu,
-                      int nesterov, cudaStream_t st) {
+                      int nesterov, int stage_only, cudaStream_t st) {
     if (ra.total == 0) return cudaSuccess;
     note_launch();
     const int grid = resident_grid(f0_kernel<kVecPerStep>, kThreads, tiles_of(ra.total));
-    f0_kernel<kVecPerStep><<<grid, kThreads, 0, st>>>(ra, m, g, u, u_stage, mu, nesterov);
+    f0_kernel<kVecPerStep><<<grid, kThreads, 0, st>>>(ra, m, g, u, u_stage, mu, nesterov, stage_only);
     return cudaGetLastError();
 }
 

@@ -352,7 +352,7 @@ struct hm_muon_plan {
     std::vector<Range> seg_tab, gather_tab;
     mutable std::vector<Range> f2_tab;
     std::vector<std::pair<int, int>> f2_shape;  // (rows, cols) of each f2 entry's unit
-    // HM_STAGE_SKIP_V: the f2 entries of units the last product cannot update
+    // HM_STAGE_SCRATCH: the f2 entries of units the last product cannot update
     // itself, and every unit's fragments for the ones it can
     mutable std::vector<Range> f2r_tab;
     std::vector<std::pair<int, int>> f2r_shape;
@@ -767,10 +767,14 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                                        void* workspace, size_t workspace_bytes, int stages, void* stream) {
     if (!p || !b || !hp || stages < 0 || stages > HM_STAGE_STEP) return HM_ERR_ARG;
     const bool fused = stages & HM_STAGE_FUSED;
-    const bool skip_v = stages & HM_STAGE_SKIP_V;
-    // v may stay unwritten only when the same call runs every stage that reads it
-    const int skip_needs = HM_STAGE_NS | HM_STAGE_F2 | HM_STAGE_REQUANT | HM_STAGE_FUSED;
-    if (skip_v && (stages & skip_needs) != skip_needs) return HM_ERR_ARG;
+    // u and v as scratch: the fused passes only, and v may stay unwritten only
+    // when the same call runs every stage that reads it
+    const bool skip_v = stages & HM_STAGE_SCRATCH;
+    const int v_needs = HM_STAGE_NS | HM_STAGE_F2 | HM_STAGE_REQUANT;
+    if (skip_v && (!fused || ((stages & HM_STAGE_NS) && (stages & v_needs) != v_needs))) return HM_ERR_ARG;
+    // the last products update the kNsEpiUpdate units themselves only when this
+    // call also runs f2 + G for the rest
+    const bool epi_update = skip_v && (stages & HM_STAGE_NS);
     if (fused) {
         // the fused passes cross stage boundaries: f0 + gather, and f2 + G
         const int front = stages & (HM_STAGE_F0 | HM_STAGE_GATHER);
@@ -801,12 +805,15 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
     if (fused && (stages & HM_STAGE_F0)) {
         // f0 writes u of straddling fragments into their staging as well
         RangeArgs ra = device_ranges(ws, p->off_f0x, p->f0x_tab);
-        if (hm::launch_f0(ra, b->m, b->g, b->u, u_stage, hp->momentum, hp->nesterov, s) != cudaSuccess)
+        // with v skipped, u of straddling units goes to their staging only: the
+        // Newton-Schulz stage reads it there and nothing reads the root copy
+        if (hm::launch_f0(ra, b->m, b->g, b->u, u_stage, hp->momentum, hp->nesterov, skip_v, s) != cudaSuccess)
             return HM_ERR_CUDA;
     }
     if (!fused && (stages & HM_STAGE_F0)) {
         RangeArgs ra = device_ranges(ws, p->off_seg, p->seg_tab);
-        if (hm::launch_f0(ra, b->m, b->g, b->u, nullptr, hp->momentum, hp->nesterov, s) != cudaSuccess) return HM_ERR_CUDA;
+        if (hm::launch_f0(ra, b->m, b->g, b->u, nullptr, hp->momentum, hp->nesterov, 0, s) != cudaSuccess)
+            return HM_ERR_CUDA;
     }
     if (!fused && (stages & HM_STAGE_GATHER) && !p->gather_tab.empty()) {
         RangeArgs ra = device_ranges(ws, p->off_gather, p->gather_tab);
@@ -876,7 +883,7 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g3.group_m = c.mp / 128;  // column bands: each X panel is fetched once per unit
                 g3.err = g1.err;
                 g3.pace = g1.pace;
-                if (last && skip_v) {
+                if (last && epi_update) {
                     // f2 and G of the kNsEpiUpdate units in this product's epilogue
                     g3.fuse_update = 1;
                     g3.decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
@@ -907,10 +914,10 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
     }
     if (fused && (stages & HM_STAGE_F2)) {
         // f2 and G in one pass: the new w of every element is quantized as it is
-        // written (with HM_STAGE_SKIP_V only for units the last product left)
-        const std::vector<Range>& tab = skip_v ? p->f2r_tab : p->f2_tab;
+        // written (with HM_STAGE_SCRATCH only for units the last product left)
+        const std::vector<Range>& tab = epi_update ? p->f2r_tab : p->f2_tab;
         if (!tab.empty()) {
-            RangeArgs ra = device_ranges(ws, skip_v ? p->off_f2r : p->off_f2, tab);
+            RangeArgs ra = device_ranges(ws, epi_update ? p->off_f2r : p->off_f2, tab);
             const float decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
             if (hm::launch_f2_requant(ra, b->w, b->v, v_stage, b->q, b->s, decay, hp->weight_decay != 0.f, s) !=
                 cudaSuccess)

@@ -179,8 +179,9 @@ inline int resident_grid(Kernel kernel, int threads, int64_t items) {
 }
 int32_t* device_error_word();
 
+// stage_only: ranges flagged for the staging write u there only (not in the u root)
 cudaError_t launch_f0(const RangeArgs& ra, float* m, const float* g, uint16_t* u, uint16_t* u_stage,
-                      float mu, int nesterov, cudaStream_t st);
+                      float mu, int nesterov, int stage_only, cudaStream_t st);
 cudaError_t launch_copy_bf16(const RangeArgs& ra, const uint16_t* src, uint16_t* dst, cudaStream_t st);
 cudaError_t launch_f2(const RangeArgs& ra, float* w, const float* v_root, const float* v_stage,
                       float decay, int has_decay, cudaStream_t st);

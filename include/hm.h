@@ -219,16 +219,20 @@ typedef struct {  /* device roots, each in the chain's emulated layout */
  * q, s equal those of the unfused stages bit for bit. */
 #define HM_STAGE_FUSED   32
 #define HM_STAGE_ALL_FUSED 63
-/* v as scratch (section 3.1, EG1: v is an update-scoped intermediate that only
- * f2 consumes): with HM_STAGE_SKIP_V the last Newton-Schulz product of every
+/* u and v as scratch (section 3.1, EG1: both are update-scoped intermediates,
+ * u consumed by f1 and v by f2).  HM_STAGE_SCRATCH requires HM_STAGE_FUSED,
+ * and NS only together with F2 and REQUANT (else HM_ERR_ARG).  With F0, the u
+ * of straddling units is written to their staging only (the u root keeps its
+ * previous contents there).  With NS, the last Newton-Schulz product of every
  * unit whose cols and fragments are multiples of HM_MX_BLOCK applies f2 and G
  * to that unit in its epilogue, reading w and writing w, q and s directly, and
- * stores no v for it; the fused F2 + REQUANT pass then covers only the other
- * units.  Requires NS, F2, REQUANT and FUSED in the same call (else
- * HM_ERR_ARG).  w, q, s (and m, u) equal those of HM_STAGE_ALL_FUSED bit for
- * bit; v keeps its previous contents for the units updated in the epilogue.
- * HM_STAGE_STEP is the whole update phase in this fastest form. */
-#define HM_STAGE_SKIP_V  64
+ * stores no v for it (v keeps its previous contents); the fused F2 + REQUANT
+ * pass then covers only the other units (a call with F2 and REQUANT but without
+ * NS runs the pass over every unit, from v).  m, w, q, s and the u of local units
+ * equal those of HM_STAGE_ALL_FUSED bit for bit.  HM_STAGE_STEP is the whole
+ * update phase in this fastest form; it may also be split into
+ * F0 | GATHER | FUSED | SCRATCH and NS | F2 | REQUANT | FUSED | SCRATCH. */
+#define HM_STAGE_SCRATCH 64
 #define HM_STAGE_STEP    127
 
 /* Runs the selected stages, in the order above, on `stream`.  u and v of

@@ -136,12 +136,22 @@ def _logical_v(hm, s, cfg):
 
 def _epilogue_updated(cfg, i):
     """Units whose last Newton-Schulz product applies f2 and G itself under
-    HM_STAGE_SKIP_V: every MX block a piece of one row (cols a multiple of 32;
+    HM_STAGE_SCRATCH: every MX block a piece of one row (cols a multiple of 32;
     the test chains' fragments are 32-aligned)."""
     return cfg.units[i].cols % 32 == 0
 
 
+def _logical_u(hm, s, cfg):
+    """u in logical order, straddling units from their staging."""
+    u = s.fetch("u").numpy().view(np.uint16).copy()
+    for i, un in enumerate(cfg.units):
+        if not hm.muon_plan_unit(s.plan, i)["local"]:
+            u[un.offset:un.offset + un.numel] = s.staging(i)[0].cpu().numpy().view(np.uint16)
+    return u
+
+
 V_UNTOUCHED = np.uint32(0x7FC0ABCD)  # a NaN payload no update produces
+U_UNTOUCHED = np.uint16(0xFFB1)      # a bf16 NaN pattern
 
 
 @pytest.mark.parametrize("name,variant", [("tiny", "plain"), ("tiny_ragged", "plain"), ("mixed", "plain"),
@@ -153,13 +163,16 @@ def test_fused_update_equals_unfused(hm, dev, name, variant):
     consecutive updates; its w is f2 of the unfused v.  HM_STAGE_STEP (f2
     and G in the last product's epilogue, v skipped) gives the same m, u, w,
     q, s bit for bit, writes v only for the units it cannot update in the
-    epilogue (cols not a multiple of 32) and leaves the others' v as it was."""
+    epilogue (cols not a multiple of 32) and leaves the others' v as it was;
+    it writes the u of straddling units to their staging only."""
     if name == "moe_small":
         cfg = workloads.scaled_muon("moe_small", [(256, 384, None)] * 6 + [(384, 256, None)] * 3, so=8, sw=4, sg=4)
         cfg.edge_shift = workloads.ragged_shift(8, 300, seed=5)
     elif name == "ragged_n":
         # transposed (100 x 64) and ragged (cols 100, 72, 80) units side by side
-        cfg = workloads.scaled_muon("ragged_n", [(64, 100, None), (100, 64, None), (32, 72, None), (48, 80, None),
+        # (48 x 80 straddles a rank edge and stays on the path through v; 160 x 64
+        # and 64 x 160 straddle and are updated in the last product)
+        cfg = workloads.scaled_muon("ragged_n", [(64, 100, None), (32, 72, None), (48, 80, None), (100, 64, None),
                                                  (160, 64, None), (64, 160, None)], so=4, sw=2, sg=2)
     else:
         cfg = workloads.get(name)
@@ -169,6 +182,7 @@ def test_fused_update_equals_unfused(hm, dev, name, variant):
     grads = [data["g"], workloads.gaussian(cfg.numel, cfg.g_std, seed=19)]
     m0 = workloads.gaussian(cfg.numel, 1e-3, seed=18)
     v_mark = np.full(cfg.numel, V_UNTOUCHED, dtype=np.uint32).view(np.float32)
+    u_mark = np.full(cfg.numel, U_UNTOUCHED, dtype=np.uint16)
     results = {}
     for stages in (hm.HM_STAGE_ALL, hm.HM_STAGE_ALL_FUSED, hm.HM_STAGE_STEP):
         s = _session(cfg, dev)
@@ -178,9 +192,11 @@ def test_fused_update_equals_unfused(hm, dev, name, variant):
         for g in grads:
             s.load("g", g)
             s.load("v", v_mark)
+            s.load("u", u_mark)
             s.run(_hp(cfg.muon), stages)
             torch.cuda.synchronize()
             out = {k: s.fetch(k).numpy() for k in ("m", "u", "w", "q", "s")}
+            out["u_logical"] = _logical_u(hm, s, cfg)
             out["v"] = _logical_v(hm, s, cfg)
             out["v_root"] = s.fetch("v").numpy()
             per_step.append(out)
@@ -197,13 +213,19 @@ def test_fused_update_equals_unfused(hm, dev, name, variant):
             if a.dtype == np.float32:
                 a, b = a.view(np.uint32), b.view(np.uint32)
             assert np.array_equal(a, b), f"fused {k} differs"
-        for k in ("m", "u", "w", "q", "s"):
+        for k in ("m", "u_logical", "w", "q", "s"):
             a, b = ref[k], step[k]
             if a.dtype == np.float32:
                 a, b = a.view(np.uint32), b.view(np.uint32)
             assert np.array_equal(a, b), f"HM_STAGE_STEP {k} differs"
+        assert np.array_equal(ref["u_logical"], ref["u"].view(np.uint16))
         for i, un in enumerate(cfg.units):
             sl = slice(un.offset, un.offset + un.numel)
+            u_root = step["u"][sl].view(np.uint16)
+            if local[i]:
+                assert np.array_equal(u_root, ref["u"][sl].view(np.uint16)), f"unit {i} u"
+            else:
+                assert (u_root == U_UNTOUCHED).all(), f"unit {i}: u root written"
             if not epi[i]:
                 assert np.array_equal(step["v"][sl].view(np.uint32), ref["v"][sl].view(np.uint32)), f"unit {i} v"
             elif local[i]:
@@ -226,10 +248,12 @@ def test_fused_stage_sets_are_validated(hm, dev):
     hp = _hp(cfg.muon)
     for bad in (hm.HM_STAGE_F0 | hm.HM_STAGE_FUSED, hm.HM_STAGE_GATHER | hm.HM_STAGE_FUSED,
                 hm.HM_STAGE_NS | hm.HM_STAGE_F2 | hm.HM_STAGE_FUSED, hm.HM_STAGE_REQUANT | hm.HM_STAGE_FUSED,
-                # v may be skipped only when the same call consumes it
-                hm.HM_STAGE_ALL | hm.HM_STAGE_SKIP_V, hm.HM_STAGE_NS | hm.HM_STAGE_SKIP_V,
-                hm.HM_STAGE_NS | hm.HM_STAGE_F2 | hm.HM_STAGE_REQUANT | hm.HM_STAGE_SKIP_V,
-                hm.HM_STAGE_STEP + 1):
+                # u and v as scratch: fused passes only, and v skipped only when the
+                # same call consumes it
+                hm.HM_STAGE_ALL | hm.HM_STAGE_SCRATCH, hm.HM_STAGE_NS | hm.HM_STAGE_SCRATCH,
+                hm.HM_STAGE_NS | hm.HM_STAGE_FUSED | hm.HM_STAGE_SCRATCH,
+                hm.HM_STAGE_NS | hm.HM_STAGE_F2 | hm.HM_STAGE_REQUANT | hm.HM_STAGE_SCRATCH,
+                hm.HM_STAGE_F0 | hm.HM_STAGE_GATHER | hm.HM_STAGE_SCRATCH, hm.HM_STAGE_STEP + 1):
         st = hm.lib().muon_update_units(C.c_void_p(s.plan), C.byref(s.bufs), C.byref(hp), C.c_void_p(s.ws),
                                         s.ws_bytes, bad, None)
         assert st == hm.HM_ERR_ARG
