@@ -184,7 +184,15 @@ def test_fused_update_equals_unfused(hm, dev, name, variant):
     v_mark = np.full(cfg.numel, V_UNTOUCHED, dtype=np.uint32).view(np.float32)
     u_mark = np.full(cfg.numel, U_UNTOUCHED, dtype=np.uint16)
     results = {}
-    for stages in (hm.HM_STAGE_ALL, hm.HM_STAGE_ALL_FUSED, hm.HM_STAGE_STEP):
+    F, SC = hm.HM_STAGE_FUSED, hm.HM_STAGE_SCRATCH
+    front = hm.HM_STAGE_F0 | hm.HM_STAGE_GATHER | F
+    back = hm.HM_STAGE_F2 | hm.HM_STAGE_REQUANT | F
+    plans = {"all": [hm.HM_STAGE_ALL], "fused": [hm.HM_STAGE_ALL_FUSED], "step": [hm.HM_STAGE_STEP],
+             # the benchmark's split of HM_STAGE_STEP into two calls
+             "step2": [front | SC, hm.HM_STAGE_NS | back | SC],
+             # scratch u, but Newton-Schulz alone: v for every unit, then f2 + G over all
+             "step3": [front | SC, hm.HM_STAGE_NS, back | SC]}
+    for name_, calls in plans.items():
         s = _session(cfg, dev)
         s.load("w", data["w"])
         s.load("m", m0)
@@ -193,7 +201,8 @@ def test_fused_update_equals_unfused(hm, dev, name, variant):
             s.load("g", g)
             s.load("v", v_mark)
             s.load("u", u_mark)
-            s.run(_hp(cfg.muon), stages)
+            for stages in calls:
+                s.run(_hp(cfg.muon), stages)
             torch.cuda.synchronize()
             out = {k: s.fetch(k).numpy() for k in ("m", "u", "w", "q", "s")}
             out["u_logical"] = _logical_u(hm, s, cfg)
@@ -202,12 +211,23 @@ def test_fused_update_equals_unfused(hm, dev, name, variant):
             per_step.append(out)
         assert all(s.canary_intact().values())
         assert hm.hm_device_error() == 0
-        results[stages] = per_step
+        results[name_] = per_step
         epi = [_epilogue_updated(cfg, i) for i in range(len(cfg.units))]
         local = [hm.muon_plan_unit(s.plan, i)["local"] for i in range(len(cfg.units))]
         s.close()
     w_prev = data["w"]
-    for ref, got, step in zip(results[hm.HM_STAGE_ALL], results[hm.HM_STAGE_ALL_FUSED], results[hm.HM_STAGE_STEP]):
+    for k_step in range(len(grads)):
+        # the split forms leave exactly what their one-call counterparts leave
+        for name_, twin in (("step2", "step"), ("step3", "step")):
+            a, b = results[name_][k_step], results[twin][k_step]
+            for k in ("m", "u", "u_logical", "w", "q", "s"):
+                x, y = a[k], b[k]
+                if x.dtype == np.float32:
+                    x, y = x.view(np.uint32), y.view(np.uint32)
+                assert np.array_equal(x, y), f"{name_} {k} differs"
+        assert np.array_equal(results["step3"][k_step]["v"].view(np.uint32),
+                              results["all"][k_step]["v"].view(np.uint32)), "step3 v"
+    for ref, got, step in zip(results["all"], results["fused"], results["step"]):
         for k in ("m", "u", "v", "w", "q", "s"):
             a, b = ref[k], got[k]
             if a.dtype == np.float32:
