@@ -77,11 +77,11 @@ def straddling_elems(cfg, plan_info) -> int:
 
 
 # DRAM bytes (read + write) of one Newton-Schulz stage of the Video-DiT x8
-# workload with f2 and G folded into its last products (norm, prepare and 30
+# workload with f2 and G folded into its last products (prepare, norm and 30
 # GEMM launches of the timed update), from
 # profiles/video_dit_launch_list_dram.md, valid for the kernel source it was
 # measured on (sha256 prefix of hm_ns.cu).
-NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.799e+11, "hm_ns_sha256": "6fab17f40d136d39"}
+NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.741e+11, "hm_ns_sha256": "f059975228b5c2bf"}
 
 
 def ns_stage_traffic(cfg):

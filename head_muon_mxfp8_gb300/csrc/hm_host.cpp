@@ -316,7 +316,6 @@ extern "C" void chain_destroy(hm_chain* c) { delete c; }
 // ============================================================================
 namespace {
 
-constexpr int64_t kPartLen = 65536;     // elements per norm partial sum
 constexpr size_t kWsAlign = 1024;
 
 struct UnitPlan {
@@ -440,8 +439,6 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
         c.np = static_cast<int32_t>(round_up(c.n, 64));
         c.n_units = static_cast<int32_t>(members[k].size());
         c.first_unit = static_cast<int32_t>(p->ns_units.size());
-        int64_t ne = static_cast<int64_t>(c.m) * c.n;
-        c.part_len = static_cast<int32_t>(std::min<int64_t>(kPartLen, round_up(ne, 8)));
         // A = X X^T and B = bA + cAA are symmetric: only output tiles with an
         // element on or above the diagonal are computed (the epilogue mirrors
         // them).  Order: bands of 8 tile-rows, column by column in a band.
@@ -465,7 +462,7 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
             c.pair_tiles = static_cast<int32_t>(tab2.size());
             p->pair_tab.push_back(tab2);
         }
-        c.parts = static_cast<int32_t>((ne + c.part_len - 1) / c.part_len);
+        c.parts = (c.np / 64) * (c.mp / 64);  // one sum of squares per 64 x 64 tile of X
         for (int i : members[k]) {
             const hm_unit_desc& u = units[i];
             const UnitPlan& q = p->up[i];
@@ -831,9 +828,10 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
             const NsClassDev& c = p->classes[k];
             const ClassMaps& mp = p->maps[k];
             const NsUnit* units_dev = reinterpret_cast<const NsUnit*>(ws + p->off_nsu) + c.first_unit;
-            if (hm::launch_ns_norm(c, units_dev, b->u, u_stage, ws, hp->eps, s) != cudaSuccess ||
-                hm::launch_ns_prepare(c, units_dev, b->u, u_stage, ws, s) != cudaSuccess)
+            if (hm::launch_ns_prepare(c, units_dev, b->u, u_stage, ws, s) != cudaSuccess ||
+                hm::launch_ns_norm(c, ws, hp->eps, s) != cudaSuccess)
                 return HM_ERR_CUDA;
+            const float* inv = reinterpret_cast<const float*>(ws + c.inv_off);
             auto bf = [&](size_t off) { return reinterpret_cast<uint16_t*>(ws + off); };
             int cur = 0;
             for (int it = 0; it < hp->ns_steps; ++it) {
@@ -851,6 +849,7 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g1.tab_len = c.sym_tiles;
                 g1.sym = 1;
                 g1.inject_no_ready = inject ? 1 : 0;
+                g1.unit_scale = it == 0 ? inv : nullptr;  // X0 is u itself: A = s^2 u u^T
                 inject = false;
                 // classes with at least 256 rows run on CTA pairs (256 x 256 tiles)
                 const bool pair = c.mp >= 256;
@@ -864,6 +863,7 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g1.inject_no_ready = 0;
 
                 hm::GemmParams g2 = g1;
+                g2.unit_scale = nullptr;
                 g2.K = c.mp;
                 g2.epi = hm::kEpiPoly; g2.alpha = hp->ns_c; g2.beta = hp->ns_b;
                 g2.add = bf(c.a_off); g2.add_us = g1.out_us; g2.ld_add = c.mp;
@@ -883,6 +883,7 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g3.group_m = c.mp / 128;  // column bands: each X panel is fetched once per unit
                 g3.err = g1.err;
                 g3.pace = g1.pace;
+                g3.unit_scale = it == 0 ? inv : nullptr;  // X1 = s (a u + B u)
                 if (last && epi_update) {
                     // f2 and G of the kNsEpiUpdate units in this product's epilogue
                     g3.fuse_update = 1;

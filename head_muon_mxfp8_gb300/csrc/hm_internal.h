@@ -76,8 +76,7 @@ struct NsClassDev {
     int32_t m, n, mp, np;
     int32_t n_units;
     int32_t first_unit;  // into the NsUnit table
-    int32_t parts;       // norm partial sums per unit
-    int32_t part_len;    // elements per partial (multiple of 8)
+    int32_t parts;       // norm partial sums per unit: one per 64 x 64 tile of X
     size_t x_off[2], a_off, b_off, part_off, inv_off;  // workspace bytes
     int32_t sym_tiles;   // tiles of the mp x mp output on or above the diagonal
     size_t sym_off;      // workspace bytes: their (tm << 16 | tn) list, L2-friendly order
@@ -112,6 +111,9 @@ struct GemmParams {
     int32_t inject_no_ready;  // failure test: never signal an accumulator as ready
     int32_t* pace;            // CTA-pair kernel: 2 device ints (tiles issued, pairs done), zero between
                               // launches; nullptr = pairs run unpaced
+    const float* unit_scale;  // first iteration: s = 1 / (||u|| + eps) per unit, X0 being u itself:
+                              // the Gram output is scaled by s^2, the B X output (acc + beta*add) by s;
+                              // nullptr = none
     // final product with the update folded in (units flagged kNsEpiUpdate):
     // w <- w*decay - step*v and G on the new w, v itself never stored
     int32_t fuse_update;
@@ -204,10 +206,11 @@ struct RsArgs {
 };
 cudaError_t launch_reduce_scatter(const RangeArgs& ra, const RsArgs& a, float* g, cudaStream_t st);
 
-cudaError_t launch_ns_norm(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
-                           const uint16_t* u_stage, char* ws, float eps, cudaStream_t st);
+// X0 (u itself, laid out and padded) and the per-tile sums of squares of u;
+// then 1 / (||u|| + eps) per unit from those sums
 cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
                               const uint16_t* u_stage, char* ws, cudaStream_t st);
+cudaError_t launch_ns_norm(const NsClassDev& c, char* ws, float eps, cudaStream_t st);
 // b_mn: the B operand is MN-major (its map has 64 x 64 boxes, N innermost)
 cudaError_t launch_ns_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p,
                            int bn, int b_mn, cudaStream_t st);

@@ -22,11 +22,11 @@ namespace {
 
 constexpr int kMaxM = HM_NOALLOC_MAX_MIN_DIM;   // padded Gram size of the scratch
 constexpr int kMaxN = HM_NOALLOC_MAX_MAX_DIM;
-constexpr int kPartLen = 65536;
 constexpr size_t kSlot = 1024;
 constexpr size_t kXBytes = static_cast<size_t>(kMaxM) * kMaxN * 2;
 constexpr size_t kABytes = static_cast<size_t>(kMaxM) * kMaxM * 2;
-constexpr size_t kPartsBytes = ((static_cast<size_t>(kMaxM) * kMaxN / kPartLen + 1) * 4 + kSlot - 1) / kSlot * kSlot;
+// one norm partial per 64 x 64 tile of X
+constexpr size_t kPartsBytes = (static_cast<size_t>(kMaxM / 64) * (kMaxN / 64) * 4 + kSlot - 1) / kSlot * kSlot;
 // layout: unit descriptor | X0 | X1 | A | B | partials | 1/norm
 constexpr size_t kOffUnit = 0;
 constexpr size_t kOffX0 = kSlot;
@@ -124,9 +124,7 @@ extern "C" hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int3
     c.mp = kMaxM;
     c.np = (n + 63) / 64 * 64;
     c.n_units = 1;
-    const int64_t ne = static_cast<int64_t>(m) * n;
-    c.part_len = static_cast<int32_t>(ne < kPartLen ? (ne + 7) / 8 * 8 : kPartLen);
-    c.parts = static_cast<int32_t>((ne + c.part_len - 1) / c.part_len);
+    c.parts = (c.np / 64) * (c.mp / 64);
     c.x_off[0] = kOffX0;
     c.x_off[1] = kOffX1;
     c.a_off = kOffA;
@@ -149,9 +147,10 @@ extern "C" hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int3
     hm::note_launch();
     write_unit_kernel<<<1, 1, 0, st>>>(unit_dev, unit);
     if (cudaGetLastError() != cudaSuccess) return HM_ERR_CUDA;
-    if (hm::launch_ns_norm(c, unit_dev, u, nullptr, ws, hp->eps, st) != cudaSuccess ||
-        hm::launch_ns_prepare(c, unit_dev, u, nullptr, ws, st) != cudaSuccess)
+    if (hm::launch_ns_prepare(c, unit_dev, u, nullptr, ws, st) != cudaSuccess ||
+        hm::launch_ns_norm(c, ws, hp->eps, st) != cudaSuccess)
         return HM_ERR_CUDA;
+    const float* inv = reinterpret_cast<const float*>(ws + c.inv_off);
     auto bf = [&](size_t off) { return reinterpret_cast<uint16_t*>(ws + off); };
     int cur = 0;
     for (int it = 0; it < hp->ns_steps; ++it) {
@@ -160,9 +159,11 @@ extern "C" hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int3
         g1.epi = hm::kEpiGram; g1.alpha = 1.f; g1.beta = 0.f;
         g1.out = bf(c.a_off); g1.out_us = static_cast<int64_t>(c.mp) * c.mp; g1.ld_out = c.mp;
         g1.err = hm::device_error_word();
+        g1.unit_scale = it == 0 ? inv : nullptr;  // X0 is u itself: A = s^2 u u^T
         if (hm::launch_ns_gemm(x_map[cur], x_map[cur], g1, 128, 0, st) != cudaSuccess) return HM_ERR_CUDA;
 
         hm::GemmParams g2 = g1;
+        g2.unit_scale = nullptr;
         g2.K = c.mp;
         g2.epi = hm::kEpiPoly; g2.alpha = hp->ns_c; g2.beta = hp->ns_b;
         g2.add = bf(c.a_off); g2.add_us = g1.out_us; g2.ld_add = c.mp;
@@ -178,6 +179,7 @@ extern "C" hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int3
         g3.ns_units = unit_dev; g3.v_root = v; g3.v_stage = nullptr;
         g3.m_real = m; g3.n_real = n;
         g3.err = g1.err;
+        g3.unit_scale = it == 0 ? inv : nullptr;  // X1 = s (a u + B u)
         if (hm::launch_ns_gemm(b_map, x_mn[cur], g3, bn3, 1, st) != cudaSuccess) return HM_ERR_CUDA;
         cur ^= 1;
     }

@@ -10,6 +10,10 @@
 // A, B and X are rounded to bf16 after each product (fp32 accumulation in
 // TMEM); the last product is written to v in fp32 or, when the caller folds
 // f2 and G into it, applied to w and quantized to (q, s) without storing v.
+// X0 is stored as u itself (exact in bf16) and s = 1 / (||u||_F + eps) enters
+// the first iteration's epilogues: A = s^2 (u u^T), X1 = s (a u + B u) -- the
+// same products with the scale applied in fp32 after the sum instead of
+// rounding s u to bf16 first.
 //
 // Layout in the workspace, per shape class of U units:
 //   X[2]   bf16 [U][mp][np]   (ping-pong)
@@ -44,79 +48,59 @@ namespace hm {
 namespace {
 
 // ---------------------------------------------------------------------------
-// Frobenius norm: per-unit partial sums of squares, then 1 / (sqrt + eps).
+// Frobenius norm: the prepare pass below leaves one sum of squares of u per
+// 64 x 64 tile of X; this kernel adds a unit's tiles in a fixed order and
+// writes 1 / (sqrt + eps).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) ns_norm_partial_kernel(const NsUnit* __restrict__ units,
-                                                               const uint16_t* __restrict__ u_root,
-                                                               const uint16_t* __restrict__ u_stage,
-                                                               float* __restrict__ partials, int parts,
-                                                               int part_len) {
-    const NsUnit nu = units[blockIdx.y];
-    const uint16_t* src = ((nu.flags & kNsUStaged) ? u_stage : u_root) + nu.u_off;
-    const int64_t numel = static_cast<int64_t>(nu.rows) * nu.cols;
-    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * part_len;
-    const int64_t b1 = min(b0 + part_len, numel);
-    float acc = 0.f;
-    for (int64_t i = b0 + threadIdx.x * 8; i < b1; i += 256 * 8) {
-        const uint4 x = __ldg(reinterpret_cast<const uint4*>(src + i));
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
-            acc = fmaf(lo, lo, acc);
-            acc = fmaf(hi, hi, acc);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    __shared__ float red[8];
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float s = 0.f;
-        for (int k = 0; k < 8; ++k) s += red[k];
-        partials[static_cast<int64_t>(blockIdx.y) * parts + blockIdx.x] = s;
-    }
-}
+constexpr int kNormThreads = 256;
 
-__global__ void ns_norm_final_kernel(const float* __restrict__ partials, int parts, float* __restrict__ inv,
-                                     float eps, int n_units) {
-    const int unit = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (unit >= n_units) return;
+__global__ void __launch_bounds__(kNormThreads) ns_norm_final_kernel(const float* __restrict__ partials, int parts,
+                                                                     float* __restrict__ inv, float eps) {
+    // one CTA per unit: thread t adds tiles t, t + 256, .., then a shuffle tree
+    // per warp and the 8 warp sums in order -- the same order on every call
+    __shared__ float red[kNormThreads / 32];
+    const int unit = blockIdx.x;
+    const float* pu = partials + static_cast<int64_t>(unit) * parts;
     float s = 0.f;
-    for (int k = lane; k < parts; k += 32) s += partials[static_cast<int64_t>(unit) * parts + k];
+    for (int k = threadIdx.x; k < parts; k += kNormThreads) s += pu[k];
 #pragma unroll
     for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) inv[unit] = 1.0f / (sqrtf(s) + eps);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int k = 0; k < kNormThreads / 32; ++k) tot += red[k];
+        inv[unit] = 1.0f / (sqrtf(tot) + eps);
+    }
 }
 
 // ---------------------------------------------------------------------------
 // X0 from u: 64x64 tiles of X coordinates through shared memory.  Both the
 // read of u (in either orientation) and the write of X move 16-byte vectors
 // of 8 bf16 when the row length allows it (n, resp. m, a multiple of 8).
+// X0 is u itself (bf16, exact): the factor 1 / (||u|| + eps) enters the first
+// iteration's products instead (X X^T times its square, B X times it), so the
+// pass also leaves the tile's sum of squares of u, the norm's partial sum, and
+// u is read once.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint16_t scale_bf16(uint16_t raw, float s) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(static_cast<uint32_t>(raw) << 16) * s));
-}
-
 constexpr int kPrepThreads = 128;  // 4 of the tile's 512 16-byte chunks per thread, loads first
 
 __global__ void __launch_bounds__(kPrepThreads) ns_prepare_kernel(const NsUnit* __restrict__ units,
                                                                    const uint16_t* __restrict__ u_root,
                                                                    const uint16_t* __restrict__ u_stage,
-                                                                   const float* __restrict__ inv,
+                                                                   float* __restrict__ partials,
                                                                    uint16_t* __restrict__ X, int m, int n, int np) {
     // X orientation.  The 8-element chunk c of row r sits at chunk c ^ (r / 8):
     // the transposed path writes down a column, and without the swizzle the 8
     // rows r, r + 8, .. its lanes hit would share one bank
     __shared__ __align__(16) uint16_t T[64][64];
+    __shared__ float red[kPrepThreads / 32];
     auto tx = [](int r, int c) { return ((((c >> 3) ^ (r >> 3)) & 7) << 3) | (c & 7); };
     const int unit = blockIdx.z;
     const NsUnit nu = units[unit];
     const uint16_t* src = ((nu.flags & kNsUStaged) ? u_stage : u_root) + nu.u_off;
     const bool tr = nu.flags & kNsTransposed;
-    const float s = inv[unit];
     const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
     // u row r has length ld and 64 consecutive X entries of one tile row map to
     // 64 consecutive u entries of one u row (non-transposed) or of one u column
@@ -139,26 +123,36 @@ __global__ void __launch_bounds__(kPrepThreads) ns_prepare_kernel(const NsUnit* 
             raw[t] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
         }
     }
+    float sq = 0.f;  // this thread's 32 values, in a fixed order
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         const int v = threadIdx.x + t * kPrepThreads;
         const int a = v >> 3, b0 = (v & 7) * 8;
         const uint32_t w[4] = {raw[t].x, raw[t].y, raw[t].z, raw[t].w};
-        uint32_t e[8];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            e[2 * k] = scale_bf16(static_cast<uint16_t>(w[k] & 0xFFFFu), s);
-            e[2 * k + 1] = scale_bf16(static_cast<uint16_t>(w[k] >> 16), s);
+            const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+            sq = fmaf(lo, lo, sq);
+            sq = fmaf(hi, hi, sq);
         }
         if (!tr) {
-            *reinterpret_cast<uint4*>(&T[a][tx(a, b0)]) =
-                make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+            *reinterpret_cast<uint4*>(&T[a][tx(a, b0)]) = raw[t];
         } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) T[b0 + k][tx(b0 + k, a)] = static_cast<uint16_t>(e[k]);
+            for (int k = 0; k < 8; ++k)
+                T[b0 + k][tx(b0 + k, a)] = static_cast<uint16_t>(k & 1 ? w[k >> 1] >> 16 : w[k >> 1] & 0xFFFFu);
         }
     }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sq;
     __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int k = 0; k < kPrepThreads / 32; ++k) tot += red[k];
+        partials[static_cast<int64_t>(unit) * gridDim.x * gridDim.y + blockIdx.y * gridDim.x + blockIdx.x] = tot;
+    }
     uint16_t* xo = X + static_cast<int64_t>(unit) * gridDim.y * 64 * np;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -413,8 +407,9 @@ __device__ __forceinline__ float4* stage4(float* stage, int r, int c4) {
 }
 
 // staging += beta * addend (the aX term of the last product), in the layout
-// of load_addend_chunk: lane l holds row l/4 + 8s, columns 8(l%4)..+7.
-__device__ __forceinline__ void stage_add_addend(const GemmParams& p, float* stage, const uint4 (&a)[4]) {
+// of load_addend_chunk: lane l holds row l/4 + 8s, columns 8(l%4)..+7; the sum
+// is scaled by sc when the product carries the first iteration's unit scale.
+__device__ __forceinline__ void stage_add_addend(const GemmParams& p, float* stage, const uint4 (&a)[4], float sc) {
     const int lane = threadIdx.x & 31;
     const int cq = (lane & 3) * 8;
 #pragma unroll
@@ -425,10 +420,16 @@ __device__ __forceinline__ void stage_add_addend(const GemmParams& p, float* sta
         float4* p0 = stage4(stage, rr, cq >> 2);
         float4* p1 = stage4(stage, rr, (cq >> 2) + 1);
         const float4 y0 = *p0, y1 = *p1;
-        *p0 = make_float4(fmaf(p.beta, a8[0], y0.x), fmaf(p.beta, a8[1], y0.y), fmaf(p.beta, a8[2], y0.z),
-                          fmaf(p.beta, a8[3], y0.w));
-        *p1 = make_float4(fmaf(p.beta, a8[4], y1.x), fmaf(p.beta, a8[5], y1.y), fmaf(p.beta, a8[6], y1.z),
-                          fmaf(p.beta, a8[7], y1.w));
+        float4 z0 = make_float4(fmaf(p.beta, a8[0], y0.x), fmaf(p.beta, a8[1], y0.y), fmaf(p.beta, a8[2], y0.z),
+                                fmaf(p.beta, a8[3], y0.w));
+        float4 z1 = make_float4(fmaf(p.beta, a8[4], y1.x), fmaf(p.beta, a8[5], y1.y), fmaf(p.beta, a8[6], y1.z),
+                                fmaf(p.beta, a8[7], y1.w));
+        if (p.unit_scale) {
+            z0 = make_float4(z0.x * sc, z0.y * sc, z0.z * sc, z0.w * sc);
+            z1 = make_float4(z1.x * sc, z1.y * sc, z1.z * sc, z1.w * sc);
+        }
+        *p0 = z0;
+        *p1 = z1;
     }
 }
 
@@ -521,6 +522,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                                               float* stage, int half, uint4 (&next)[4]) {
     const int i = i_base + row;
     const int c_end = (half + 1) * (BN / 64);
+    // first iteration: the unit's scale s (Gram outputs take s^2)
+    const float usc = p.unit_scale ? p.unit_scale[u] : 1.f;
+    const float alpha_t = p.unit_scale ? p.alpha * (usc * usc) : p.alpha;
     // last product: the unit's destination once per tile
     NsUnit nu{};
     bool fuse = false;
@@ -576,6 +580,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                     const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
                     for (int t = 0; t < 8; ++t) o[t] = fmaf(p.beta, a8[t], y[t]);
+                    if (p.unit_scale) {
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) o[t] *= usc;
+                    }
                     *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(i0 + rr) * p.ld_out) = make_uint4(
                         bf16x2_bits(o[0], o[1]), bf16x2_bits(o[2], o[3]),
                         bf16x2_bits(o[4], o[5]), bf16x2_bits(o[6], o[7]));
@@ -584,7 +592,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
             }
             // last iteration: v = fp32(aX + BX) into the unit's own v location,
             // or f2 and G of the unit straight from the staging
-            stage_add_addend(p, stage, a);
+            stage_add_addend(p, stage, a, usc);
             __syncwarp();
             if (fuse) {
                 final_update_chunk(p, nu, base1, stage, i0, j0);
@@ -638,9 +646,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
             auto st4 = [&](int r, int c4) { return reinterpret_cast<float4*>(stage + r * 32 + ((c4 ^ (r & 7)) << 2)); };
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
-                *st4(lane, c4) = make_float4(__uint_as_float(r[4 * c4]) * p.alpha, __uint_as_float(r[4 * c4 + 1]) * p.alpha,
-                                             __uint_as_float(r[4 * c4 + 2]) * p.alpha,
-                                             __uint_as_float(r[4 * c4 + 3]) * p.alpha);
+                *st4(lane, c4) = make_float4(__uint_as_float(r[4 * c4]) * alpha_t, __uint_as_float(r[4 * c4 + 1]) * alpha_t,
+                                             __uint_as_float(r[4 * c4 + 2]) * alpha_t,
+                                             __uint_as_float(r[4 * c4 + 3]) * alpha_t);
             __syncwarp();
             const int cq = (lane & 3) * 8;
             if (p.epi == kEpiPoly) {
@@ -706,7 +714,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
         // full-grid outputs (the allocation-free entry point's A and B)
         float v[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * p.alpha;
+        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * alpha_t;
         if (p.epi == kEpiPoly) {
             const uint4* ap = reinterpret_cast<const uint4*>(p.add + u * p.add_us + static_cast<int64_t>(i) * p.ld_add + j0);
 #pragma unroll
@@ -1172,27 +1180,19 @@ cudaError_t launch_gemm_bn(const CUtensorMap& tma, const CUtensorMap& tmb, const
 
 }  // namespace
 
-cudaError_t launch_ns_norm(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
-                           const uint16_t* u_stage, char* ws, float eps, cudaStream_t st) {
-    float* partials = reinterpret_cast<float*>(ws + c.part_off);
-    float* inv = reinterpret_cast<float*>(ws + c.inv_off);
-    dim3 g1(c.parts, c.n_units);
-    note_launch();
-    ns_norm_partial_kernel<<<g1, 256, 0, st>>>(units_dev, u_root, u_stage, partials, c.parts, c.part_len);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    note_launch();
-    ns_norm_final_kernel<<<(c.n_units + 7) / 8, 256, 0, st>>>(partials, c.parts, inv, eps, c.n_units);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
                               const uint16_t* u_stage, char* ws, cudaStream_t st) {
     dim3 g(c.np / 64, c.mp / 64, c.n_units);
     note_launch();
-    ns_prepare_kernel<<<g, kPrepThreads, 0, st>>>(units_dev, u_root, u_stage,
-                                                  reinterpret_cast<const float*>(ws + c.inv_off),
+    ns_prepare_kernel<<<g, kPrepThreads, 0, st>>>(units_dev, u_root, u_stage, reinterpret_cast<float*>(ws + c.part_off),
                                                   reinterpret_cast<uint16_t*>(ws + c.x_off[0]), c.m, c.n, c.np);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ns_norm(const NsClassDev& c, char* ws, float eps, cudaStream_t st) {
+    note_launch();
+    ns_norm_final_kernel<<<c.n_units, kNormThreads, 0, st>>>(reinterpret_cast<const float*>(ws + c.part_off), c.parts,
+                                                             reinterpret_cast<float*>(ws + c.inv_off), eps);
     return cudaGetLastError();
 }
 
