@@ -49,11 +49,12 @@ def ns_flops(cfg, steps: int) -> float:
 
 def ns_executed_flops(cfg, steps: int) -> float:
     """Tensor-core FLOP the kernels actually issue per update, by the kernel
-    a shape class runs on:
-    - m <= 128 (single-CTA GEMMs): 128 x 128 tiles on or above the diagonal
-      for X X^T and bA + cAA, 128 x BN tiles of B X, K padded to 64;
-    - m > 128 (CTA pairs): 256 x 256 tiles, the upper triangle for the
-      symmetric products and the full grid of B X."""
+    a shape class runs on (Gram size mp = m rounded up to 128):
+    - single-CTA GEMMs (mp = 128, or mp not a multiple of 256): 128 x BN tiles
+      (BN = 256 once mp >= 256) on or above the diagonal for X X^T and
+      bA + cAA, 128 x BN3 tiles of B X, K padded to 64;
+    - CTA pairs (mp a multiple of 256): 256 x 256 tiles, the upper triangle
+      for the symmetric products and the full grid of B X."""
     classes = {}
     for u in cfg.units:
         key = (min(u.rows, u.cols), max(u.rows, u.cols))
@@ -61,9 +62,12 @@ def ns_executed_flops(cfg, steps: int) -> float:
     tot = 0.0
     for (m, n), cnt in classes.items():
         mp, np_ = -(-m // 128) * 128, -(-n // 64) * 64
-        if mp <= 128:
+        if mp <= 128 or mp % 256:
+            bn = 256 if mp >= 256 else 128
             bn3 = 256 if np_ >= 256 else 128
-            per_it = 2.0 * 128 * 128 * np_ + 2.0 * 128 * 128 * mp + -(-np_ // bn3) * 2.0 * 128 * bn3 * mp
+            sym = sum(1 for tm in range(mp // 128) for tn in range(-(-mp // bn)) if tn * bn + bn - 1 >= tm * 128)
+            per_it = (sym * 2.0 * 128 * bn * (np_ + mp) +
+                      (mp // 128) * -(-np_ // bn3) * 2.0 * 128 * bn3 * mp)
         else:
             t2 = -(-mp // 256)
             tri = t2 * (t2 + 1) // 2

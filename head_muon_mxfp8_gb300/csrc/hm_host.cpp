@@ -851,8 +851,10 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 g1.inject_no_ready = inject ? 1 : 0;
                 g1.unit_scale = it == 0 ? inv : nullptr;  // X0 is u itself: A = s^2 u u^T
                 inject = false;
-                // classes with at least 256 rows run on CTA pairs (256 x 256 tiles)
-                const bool pair = c.mp >= 256;
+                // classes whose Gram size is a multiple of 256 run on CTA pairs (256 x 256
+                // tiles); others keep 128-row tiles, since a pair's last tile-row would be
+                // half empty (1408-row experts: 1.5 % faster per update on single CTAs)
+                const bool pair = c.mp >= 256 && c.mp % 256 == 0;
                 if (pair) {
                     g1.tile_tab = reinterpret_cast<const int32_t*>(ws + c.pair_off);
                     g1.tab_len = c.pair_tiles;

@@ -262,7 +262,9 @@ def generate_device(cfg: Config, device, seed: Optional[int] = None):
 def mixed() -> Config:
     """A small config that exercises every path: per-head units, transposed
     and non-transposed whole matrices, a Gram size that is not a multiple of
-    128, a width that is not a multiple of 64, and ragged edges over 8 ranks."""
+    128, one that is a multiple of 128 but not of 256 (single-CTA 128 x 256
+    tiles instead of CTA pairs), a width that is not a multiple of 64, and
+    ragged edges over 8 ranks."""
     b = _ListBuilder()
     _qkv(b, "", d=512, hq=4, hkv=4, dh=64)       # 12 x (64 x 512)
     b.add("up", 1536, 512)                       # transposed, 512 x 1536
@@ -270,6 +272,8 @@ def mixed() -> Config:
     for e in range(3):
         b.add(f"e{e}", 192, 320)                 # m = 192 -> padded to 256
     b.add("odd", 96, 160)                        # n = 160 -> padded to 192
+    b.add("mid0", 384, 640)                      # Gram 384: single-CTA kernel
+    b.add("mid1", 640, 384)                      # the same class, transposed
     return Config("mixed", "test mix of unit shapes over 8 ragged ranks", "muon", b.members, b.units,
                   so=8, sw=4, sg=4, edge_shift=ragged_shift(8, 400, seed=8))
 
