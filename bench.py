@@ -467,6 +467,10 @@ def run_ours(args, cfg):
     for k, v in extra.items():
         v["frac"] = v["gbs"] / peaks["hbm_gbs"]
         kern[k] = v
+    # the same HBM rates against the nominal 8 TB/s of GB300's HBM3e
+    for v in kern.values():
+        if v.get("gbs") is not None:
+            v["frac_of_8tbs"] = v["gbs"] / 8000.0
     roofline = {"bound": "tensor", "achieved": ns_tflops, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                 "frac": ns_tflops / peaks["bf16_sustained"], "traffic": ns_stage_traffic(cfg),
                 "traffic_unit": "DRAM bytes per Newton-Schulz stage (one update), ncu",
