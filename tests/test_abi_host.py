@@ -156,6 +156,30 @@ def test_plan_rejections(hm):
     hm.chain_destroy(ch)
 
 
+def test_stage_sets_are_checked_before_any_device_work(hm):
+    """Which stage sets muon_update_units accepts is decided on the host,
+    before the workspace is looked at: rejected sets return HM_ERR_ARG,
+    accepted ones get as far as the missing upload (HM_ERR_STATE)."""
+    ch = hm.shard_chain(1024, 4, 2, 2)
+    plan = hm.muon_plan(ch, [(0, 16, 32), (512, 16, 32)])
+    bufs = hm.hm_muon_bufs(16, 16, 16, 16, 16, 16, 16)
+    hp = hm.hm_muon_hparams(0.02, 0.95, 0.0, 1e-7, 3.4445, -4.775, 2.0315, 5, 0, 0)
+    F0, GA, NS, F2, RQ = hm.HM_STAGE_F0, hm.HM_STAGE_GATHER, hm.HM_STAGE_NS, hm.HM_STAGE_F2, hm.HM_STAGE_REQUANT
+    FU, SC = hm.HM_STAGE_FUSED, hm.HM_STAGE_SCRATCH
+    accepted = [hm.HM_STAGE_ALL, hm.HM_STAGE_ALL_FUSED, hm.HM_STAGE_STEP, F0, NS, F2 | RQ, F0 | GA | FU,
+                F2 | RQ | FU, NS | F2 | RQ | FU, F0 | GA | FU | SC, NS | F2 | RQ | FU | SC, F2 | RQ | FU | SC,
+                NS | FU]
+    rejected = [-1, hm.HM_STAGE_STEP + 1, 128, F0 | FU, GA | FU, F2 | FU, RQ | FU, F0 | GA | F2 | FU,
+                hm.HM_STAGE_ALL | SC, F0 | GA | SC, NS | SC, NS | FU | SC, NS | F2 | FU | SC, NS | F2 | RQ | SC]
+    for stages in accepted + rejected:
+        st = hm.lib().muon_update_units(C.c_void_p(plan), C.byref(bufs), C.byref(hp), C.c_void_p(1 << 20), 1 << 20,
+                                        stages, None)
+        want = hm.HM_ERR_STATE if stages in accepted else hm.HM_ERR_ARG
+        assert st == want, (stages, st)
+    hm.muon_plan_destroy(plan)
+    hm.chain_destroy(ch)
+
+
 def test_data_tree_views_alias_the_root(hm):
     base = 0x10000000
     t = hm.create_data_tree(base, 1 << 20)
