@@ -244,8 +244,11 @@ typedef struct {  /* device roots, each in the chain's emulated layout */
  * captured into a CUDA graph and replayed, provided one call with the same
  * lr and alpha_mode ran outside the capture first: a change of either
  * re-uploads the per-unit step table from host memory (a copy a capture
- * cannot hold).  Replays read that table from the workspace, so a later
- * uncaptured call with a new lr also updates the graph's steps. */
+ * cannot hold).  Replays read that table (and the per-unit steps of the
+ * last products) from the workspace, so a later uncaptured call with a new
+ * lr also updates the graph's steps; the other scalars -- mu, the weight
+ * decay factor fp32(1 - lr * wd), eps, a, b, c -- are kernel arguments fixed
+ * at capture. */
 hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs* bufs,
                             const hm_muon_hparams* hp, void* workspace, size_t workspace_bytes,
                             int stages, void* stream);
