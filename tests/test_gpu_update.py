@@ -431,3 +431,35 @@ def test_newton_schulz_ragged_row_tails(hm, dev):
     assert all(s.canary_intact().values())
     assert hm.hm_device_error() == 0
     s.close()
+
+
+@pytest.mark.parametrize("steps", [1, 2])
+def test_newton_schulz_iteration_counts(hm, dev, steps):
+    """One iteration (the first iteration's 1 / (||u|| + eps) scale lands in
+    the last product's epilogue, also with f2 and G folded in) and two:
+    Newton-Schulz output against the oracle run for the same count, and
+    HM_STAGE_STEP's w, q, s equal to the pass through v bit for bit."""
+    cfg = workloads.get("mixed")
+    cfg.muon = dataclasses.replace(cfg.muon, ns_steps=steps, weight_decay=0.1, lr=float(np.float32(0.02)))
+    data = workloads.generate(cfg, seed=21)
+    m0 = workloads.gaussian(cfg.numel, 1e-3, seed=22)
+    out = {}
+    for stages in (hm.HM_STAGE_ALL, hm.HM_STAGE_STEP):
+        s = _session(cfg, dev)
+        s.load("w", data["w"])
+        s.load("g", data["g"])
+        s.load("m", m0)
+        s.run(_hp(cfg.muon), stages)
+        torch.cuda.synchronize()
+        assert hm.hm_device_error() == 0
+        out[stages] = {k: s.fetch(k).numpy() for k in ("w", "q", "s")}
+        if stages == hm.HM_STAGE_ALL:
+            check_ns(cfg, s.fetch("u").numpy().view(np.uint16), _logical_v(hm, s, cfg), cfg.muon)
+            check_f2(cfg, data["w"], _logical_v(hm, s, cfg), out[stages]["w"], cfg.muon)
+        assert all(s.canary_intact().values())
+        s.close()
+    for k in ("w", "q", "s"):
+        a, b = out[hm.HM_STAGE_ALL][k], out[hm.HM_STAGE_STEP][k]
+        if a.dtype == np.float32:
+            a, b = a.view(np.uint32), b.view(np.uint32)
+        assert np.array_equal(a, b), k
