@@ -85,7 +85,7 @@ def straddling_elems(cfg, plan_info) -> int:
 # GEMM launches of the timed update), from
 # profiles/video_dit_launch_list_dram.md, valid for the kernel source it was
 # measured on (sha256 prefix of hm_ns.cu).
-NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.741e+11, "hm_ns_sha256": "f059975228b5c2bf"}
+NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.751e+11, "hm_ns_sha256": "ed1104c8bcff3862"}
 
 
 def ns_stage_traffic(cfg):

@@ -399,11 +399,28 @@ __device__ __forceinline__ int64_t unit_root_offset(const GemmParams& p, const N
     return p.frags[f].root_off + (e - p.frags[f].unit_off);
 }
 
-// 16-byte chunk c4 of row r of a warp's 32 x 32 fp32 staging tile: chunk c4
-// of row r sits at c4 ^ (r % 8), so row-wise writes and 4-lanes-per-row reads
-// are both conflict-free.
+// A warp's 32 x 32 fp32 staging tile keeps 16-byte chunk c4 of row r at
+// chunk c4 ^ swz(r), swz(r) = (r % 8) ^ 2 (r / 8): the row-wise writes (lane r
+// writes row r), the 4-lanes-per-row reads (lanes 4k..4k+3 read row k + 8s)
+// and the column reads of the mirror and transposed paths (lane reads column
+// l/4 + 8s of rows 8(l%4) + e) all hit 32 distinct banks.
+__device__ __forceinline__ int swz(int r) { return (r & 7) ^ ((r >> 2) & 6); }
 __device__ __forceinline__ float4* stage4(float* stage, int r, int c4) {
-    return reinterpret_cast<float4*>(stage + r * 32 + ((c4 ^ (r & 7)) << 2));
+    return reinterpret_cast<float4*>(stage + r * 32 + ((c4 ^ swz(r)) << 2));
+}
+__device__ __forceinline__ float4 stage4_ld(const float* stage, int r, int c4) {
+    return *reinterpret_cast<const float4*>(stage + r * 32 + ((c4 ^ swz(r)) << 2));
+}
+// element (r, c) of the staging tile
+__device__ __forceinline__ float stage_at(const float* stage, int r, int c) {
+    return stage[r * 32 + ((((c >> 2) ^ swz(r)) << 2) | (c & 3))];
+}
+// column c of rows r0 .. r0+7 (r0 a multiple of 8, so swz(r0 + e) = e ^ r0 / 4)
+__device__ __forceinline__ void stage_col8(const float* stage, int r0, int c, float (&y)[8]) {
+    const int k0 = (c >> 2) ^ (r0 >> 2);
+    const float* base = stage + r0 * 32 + (c & 3);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = base[e * 32 + ((k0 ^ e) << 2)];
 }
 
 // staging += beta * addend (the aX term of the last product), in the layout
@@ -477,12 +494,10 @@ __device__ __forceinline__ void final_update_chunk(const GemmParams& p, const Ns
         const int kk = (lane >> 2) + 8 * s;
         float y[8];
         if (tr) {
-            // column kk of the chunk, rows cq..cq+7 (chunk c of row r sits at c ^ (r % 8))
-#pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = stage[(cq + e) * 32 + ((((kk >> 2) ^ e) << 2) | (kk & 3))];
+            stage_col8(stage, cq, kk, y);  // column kk of the chunk, rows cq..cq+7
         } else {
-            const float4 a = *reinterpret_cast<const float4*>(stage + kk * 32 + (((cq >> 2) ^ (kk & 7)) << 2));
-            const float4 b = *reinterpret_cast<const float4*>(stage + kk * 32 + ((((cq >> 2) + 1) ^ (kk & 7)) << 2));
+            const float4 a = stage4_ld(stage, kk, cq >> 2);
+            const float4 b = stage4_ld(stage, kk, (cq >> 2) + 1);
             y[0] = a.x; y[1] = a.y; y[2] = a.z; y[3] = a.w;
             y[4] = b.x; y[5] = b.y; y[6] = b.z; y[7] = b.w;
         }
@@ -557,12 +572,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
             // aX + BX through the warp's staging: the lane that holds row i parks
             // its 32 sums, then every load of the addend (and every store of X')
             // covers 8 rows x 64 contiguous bytes, 4 lanes per row, instead of
-            // 32 rows x 16 bytes.  The 32 x 32 fp32 tile keeps 16-byte chunk c of
-            // row r at chunk c ^ (r % 8), so the row-wise writes and the 4-lanes-
-            // per-row reads are both conflict-free 16-byte accesses.  (These two
-            // epilogues have no alpha: acc is B X as it stands.)
+            // 32 rows x 16 bytes; the tile's swizzle (swz above) keeps the row-wise
+            // writes and the 4-lanes-per-row reads conflict-free 16-byte accesses.
+            // (These two epilogues have no alpha: acc is B X as it stands.)
             const int lane = threadIdx.x & 31;
-            auto st4 = [&](int r, int c4) { return reinterpret_cast<float4*>(stage + r * 32 + ((c4 ^ (r & 7)) << 2)); };
+            auto st4 = [&](int r, int c4) { return stage4(stage, r, c4); };
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
                 *st4(lane, c4) = make_float4(__uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]),
@@ -632,7 +646,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                 for (int r2 = 0; r2 < 32; ++r2)
                     if (i0 + r2 < p.m_real)
                         dst[static_cast<int64_t>(i0 + r2) * p.n_real + j0 + lane] =
-                            stage[r2 * 32 + ((((lane >> 2) ^ (r2 & 7)) << 2) | (lane & 3))];
+                            stage_at(stage, r2, lane);
             }
             __syncwarp();
             continue;
@@ -643,7 +657,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
             // to (j, i), through the same swizzled staging tile: the chunk and its
             // transpose both leave as 16-byte stores of 8 rows x 16 bytes
             const int lane = threadIdx.x & 31;
-            auto st4 = [&](int r, int c4) { return reinterpret_cast<float4*>(stage + r * 32 + ((c4 ^ (r & 7)) << 2)); };
+            auto st4 = [&](int r, int c4) { return stage4(stage, r, c4); };
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
                 *st4(lane, c4) = make_float4(__uint_as_float(r[4 * c4]) * alpha_t, __uint_as_float(r[4 * c4 + 1]) * alpha_t,
@@ -700,9 +714,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
                 for (int s = 0; s < 4; ++s) {
                     const int kk = (lane >> 2) + 8 * s;
                     float y[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        y[e] = stage[(cq + e) * 32 + ((((kk >> 2) ^ e) << 2) | (kk & 3))];
+                    stage_col8(stage, cq, kk, y);
                     *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(j0 + kk) * p.ld_out + i0 + cq) = make_uint4(
                         bf16x2_bits(y[0], y[1]), bf16x2_bits(y[2], y[3]),
                         bf16x2_bits(y[4], y[5]), bf16x2_bits(y[6], y[7]));
