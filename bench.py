@@ -82,9 +82,9 @@ def straddling_elems(cfg, plan_info) -> int:
 
 # DRAM bytes (read + write) of one Newton-Schulz stage of the Video-DiT x8
 # workload with f2 and G folded into its last products (prepare, norm and 30
-# GEMM launches of the timed update), from
-# profiles/video_dit_launch_list_dram.md, valid for the kernel source it was
-# measured on (sha256 prefix of hm_ns.cu).
+# GEMM launches of the timed update), summed from an ncu launch list of
+# dram__bytes_read.sum + dram__bytes_write.sum; valid only for the kernel
+# source it was measured on (sha256 prefix of hm_ns.cu).
 NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.751e+11, "hm_ns_sha256": "ed1104c8bcff3862"}
 
 
@@ -491,15 +491,26 @@ def run_ours(args, cfg):
         cpu = {"value": cfg.numel / total, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                "sample": desc, "sample_wall_s": time.perf_counter() - t0}
 
+    resident_gb = (sess.total * 21 + sess.ws_bytes) / 1e9
+    n_classes, n_strad = info.n_classes, info.n_straddling
+    sess.close()
+    del sess
+    torch.cuda.empty_cache()
+    # ---- every shape class alone, and the other workloads (N = 1 only) ----
+    classes, configs = {}, None
+    if world == 1 and not args.skip_configs:
+        classes = ns_class_table(cfg, dev, stream, peaks)
+        configs = bench_other_configs(dev, stream, peaks)
+    kern.update(classes)
+
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16+fp32", "data": "synthetic (seeded N(0,0.02) w, N(0,1e-3) g)",
                 "config": {"workload": f"{cfg.name}: {cfg.description}", "params": P, "units": len(cfg.units),
-                           "shape_classes": info.n_classes, "straddling_units": info.n_straddling,
+                           "shape_classes": n_classes, "straddling_units": n_strad,
                            "emulated_ranks": cfg.so, "parallelism": f"replica x{world}",
-                           "l2": "inputs larger than L2 (resident state ~%.0f GB)" % (
-                               (sess.total * 21 + sess.ws_bytes) / 1e9)},
+                           "l2": "inputs larger than L2 (resident state ~%.0f GB)" % resident_gb},
                 "ns_tflops": ns_tflops, "ns_flops_per_step": flops, "ns_executed_flops_per_step": exec_flops,
                 "stages_ms": stage_ms, "through_v_stages_ms": through_v_ms, "unfused_stages_ms": unfused_ms,
                 "kernels": kern,
@@ -512,8 +523,9 @@ def run_ours(args, cfg):
                 "gpu_launches": launches, "clocks": clocks.summary()}
         if graph is not None:
             line["graph"] = graph
+        if configs is not None:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
-    sess.close()
     if dist:
         dist.barrier()
         dist.destroy_process_group()
@@ -701,6 +713,192 @@ def bench_adamw(dev, stream, steps: int = 10):
             "workload": "flat_adamw 67,108,864 fp32 params, bf16 grads (inputs larger than L2)"}
 
 
+def time_muon_update(cfg, dev, stream, steps: int, warmup: int):
+    """Times `steps` whole update phases of cfg on its own session, exactly as
+    the headline step runs (HM_STAGE_STEP as two calls, CUDA events on the
+    launching stream around each, inputs resident in HBM), with the SM clocks
+    sampled meanwhile.  The session is freed before returning."""
+    import torch
+
+    from head_muon_mxfp8_gb300 import abi
+    from head_muon_mxfp8_gb300.session import MuonSession, muon_hparams
+    sess = MuonSession.from_config(cfg, device=dev, canaries=False)
+    data = workloads.generate_device(cfg, dev, seed=cfg.seed)
+    sess.load("w", data["w"])
+    sess.load("g", data["g"])
+    sess.m.zero_()
+    del data
+    hp = muon_hparams(cfg.muon)
+    front_s = abi.HM_STAGE_F0 | abi.HM_STAGE_GATHER | abi.HM_STAGE_FUSED | abi.HM_STAGE_SCRATCH
+    ns_back = abi.HM_STAGE_STEP & ~(abi.HM_STAGE_F0 | abi.HM_STAGE_GATHER)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            sess.run(hp, abi.HM_STAGE_STEP, stream)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    launches0 = abi.hm_kernel_launches()
+    with torch.cuda.stream(stream):
+        for e in evs:
+            e[0].record(stream)
+            sess.run(hp, front_s, stream)
+            e[1].record(stream)
+            sess.run(hp, ns_back, stream)
+            e[2].record(stream)
+    launches = abi.hm_kernel_launches() - launches0
+    torch.cuda.synchronize()
+    clocks.stop()
+    if abi.hm_device_error() != 0:
+        raise RuntimeError(f"device error word set while timing {cfg.name}")
+    out = {"f0_gather_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+           "ns_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
+           "step_ms": evs[0][0].elapsed_time(evs[-1][2]) / steps,
+           "launches_per_step": launches / steps, "clocks": clocks.summary(),
+           "n_classes": int(sess.info.n_classes), "n_straddling": int(sess.info.n_straddling)}
+    sess.close()
+    del sess
+    torch.cuda.empty_cache()
+    return out
+
+
+def ns_class_table(cfg, dev, stream, peaks, steps: int = 5, warmup: int = 2):
+    """Every Newton-Schulz shape class of cfg timed alone (its members as a
+    workload of their own, the same step as the headline).  Beside the tensor
+    fractions each class reports an HBM fraction against the traffic of the
+    iteration run product by product: per iteration X X^T reads X (2mn bytes)
+    and writes A (2m^2), bA + cAA reads A and writes B (4m^2), B X reads B and
+    X and writes X' (2m^2 + 4mn); plus u in (2mn) and, for the last product
+    with f2 and G folded in, w read and written, q and s written
+    (8mn + mn + mn/32) -- per unit."""
+    classes = {}
+    for u in cfg.units:
+        k = (min(u.rows, u.cols), max(u.rows, u.cols))
+        classes[k] = classes.get(k, 0) + 1
+    if len(classes) < 2:
+        return {}
+    out = {}
+    steps_ns = cfg.muon.ns_steps
+    for (m, n), cnt in sorted(classes.items()):
+        sub = workloads.class_subset(cfg, m, n)
+        t = time_muon_update(sub, dev, stream, steps, warmup)
+        sec = t["ns_ms"] / 1e3
+        alg = ns_flops(sub, steps_ns)
+        exe = ns_executed_flops(sub, steps_ns)
+        io = cnt * (steps_ns * (6.0 * m * n + 8.0 * m * m) + 2.0 * m * n + (10.0 + 1 / 32) * m * n)
+        out[f"ns_class_{m}x{n}"] = {
+            "units": cnt, "ms": t["ns_ms"], "tflops": alg / sec / 1e12,
+            "frac": alg / sec / 1e12 / peaks["bf16_sustained"],
+            "executed_tflops": exe / sec / 1e12, "executed_frac": exe / sec / 1e12 / peaks["bf16_sustained"],
+            "hbm_bytes_product_by_product": io, "gbs": io / sec / 1e9, "hbm_frac": io / sec / 1e9 / peaks["hbm_gbs"],
+            "sm_mhz": t["clocks"]["sm_mhz"]}
+    return out
+
+
+def bench_other_configs(dev, stream, peaks, steps: int = 10, warmup: int = 3):
+    """The other workloads, each timed like the headline after its session is
+    freed: params/s of the whole update phase, the Newton-Schulz stage's
+    tensor fractions, the fused f0 + gather pass's HBM fraction, the clocks
+    seen, and the CPU oracle on a bounded sample of the same workload.  Flat
+    AdamW is one AdamW step over the 64 M shard followed by the MXFP8 requant
+    of the 64 M weights as 16384 x 4096 row-major blocks."""
+    out = {}
+    for name, k in (("tiny", 50), ("lm_layer", steps), ("moe_layer", steps)):
+        cfg = workloads.get(name)
+        t = time_muon_update(cfg, dev, stream, k, warmup)
+        P = cfg.numel
+        alg = ns_flops(cfg, cfg.muon.ns_steps)
+        exe = ns_executed_flops(cfg, cfg.muon.ns_steps)
+        sec = t["ns_ms"] / 1e3
+        t0 = time.perf_counter()
+        _, total, desc = oracle_sample_step(cfg)
+        cpu = {"value": P / total, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle", "sample": desc,
+               "sample_wall_s": time.perf_counter() - t0}
+        out[name] = {
+            "params": P, "units": len(cfg.units), "shape_classes": t["n_classes"],
+            "straddling_units": t["n_straddling"], "emulated_ranks": cfg.so, "steps": k,
+            "value": P * 1e3 / t["step_ms"], "unit": UNIT, "ms_per_step": t["step_ms"],
+            "stages_ms": {"f0_gather": t["f0_gather_ms"], "ns_f2_requant": t["ns_ms"]},
+            "ns": {"tflops": alg / sec / 1e12, "frac": alg / sec / 1e12 / peaks["bf16_sustained"],
+                   "executed_tflops": exe / sec / 1e12,
+                   "executed_frac": exe / sec / 1e12 / peaks["bf16_sustained"]},
+            "f0_gather_fused": {"gbs": 14.0 * P / (t["f0_gather_ms"] / 1e3) / 1e9,
+                                "frac": 14.0 * P / (t["f0_gather_ms"] / 1e3) / 1e9 / peaks["hbm_gbs"]},
+            "gpu_launches_per_step": t["launches_per_step"], "clocks": t["clocks"], "cpu_baseline": cpu,
+            "l2": ("inputs larger than L2" if P * 21 > 129e6 else
+                   "state fits in L2 (no flush between steps; launch-bound)")}
+    out["flat_adamw"] = bench_flat_adamw_config(dev, stream, peaks)
+    return out
+
+
+def bench_flat_adamw_config(dev, stream, peaks, steps: int = 10):
+    import torch
+
+    from head_muon_mxfp8_gb300 import abi
+    from head_muon_mxfp8_gb300.session import adamw_hparams
+    from oracle import adamw as OA
+    from oracle import mxfp8 as OX
+    cfg = workloads.flat_adamw()
+    n = cfg.numel
+    rows, k = 16384, n // 16384
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg.seed)
+    w = torch.empty(n, device=dev).normal_(0, cfg.w_std, generator=gen)
+    g = torch.empty(n, device=dev).normal_(0, cfg.g_std, generator=gen).to(torch.bfloat16)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    q = torch.empty(n, dtype=torch.uint8, device=dev)
+    sc = torch.empty(n // 32, dtype=torch.uint8, device=dev)
+    sh = int(stream.cuda_stream)
+    h = cfg.adamw
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    clocks = ClockSampler(dev.index or 0)
+    with torch.cuda.stream(stream):
+        for t in range(3):
+            abi.adamw_update_flat(w.data_ptr(), g.data_ptr(), abi.HM_BF16, m.data_ptr(), v.data_ptr(), n,
+                                  adamw_hparams(h, t + 1), sh)
+            abi.mxfp8_requant_packed(w.data_ptr(), q.data_ptr(), sc.data_ptr(), [(0, 0, 0, rows, k)], sh)
+        torch.cuda.synchronize()
+        clocks.start()
+        time.sleep(0.3)
+        for j, e in enumerate(evs):
+            e[0].record(stream)
+            abi.adamw_update_flat(w.data_ptr(), g.data_ptr(), abi.HM_BF16, m.data_ptr(), v.data_ptr(), n,
+                                  adamw_hparams(h, 4 + j), sh)
+            e[1].record(stream)
+            abi.mxfp8_requant_packed(w.data_ptr(), q.data_ptr(), sc.data_ptr(), [(0, 0, 0, rows, k)], sh)
+            e[2].record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    a_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    r_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    step_ms = evs[0][0].elapsed_time(evs[-1][2]) / steps
+    del w, g, m, v, q, sc
+    torch.cuda.empty_cache()
+    # the oracle on a 262,144-element slice (AdamW in float64, then the requant), scaled by elements
+    rng = np.random.default_rng(0)
+    ns = 1 << 18
+    t0 = time.perf_counter()
+    w0 = (rng.standard_normal(ns) * cfg.w_std).astype(np.float32)
+    g0 = (rng.standard_normal(ns) * cfg.g_std).astype(np.float32)
+    t1 = time.perf_counter()
+    w1, _, _ = OA.adamw_step(w0, g0, np.zeros(ns), np.zeros(ns), h.lr, h.beta1, h.beta2, h.eps, h.weight_decay, 1)
+    OX.requant_list(w1.astype(np.float32), [(0, ns // k, k)])
+    per_el = (time.perf_counter() - t1) / ns
+    return {"params": n, "steps": steps, "value": n * 1e3 / step_ms, "unit": UNIT, "ms_per_step": step_ms,
+            "stages_ms": {"adamw": a_ms, "mxfp8_requant": r_ms},
+            "kernels": {"adamw": {"gbs": 26.0 * n / (a_ms / 1e3) / 1e9, "bytes_per_elem": 26,
+                                  "frac": 26.0 * n / (a_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
+                        "mxfp8_requant": {"gbs": 5.03125 * n / (r_ms / 1e3) / 1e9, "bytes_per_elem": 5.03125,
+                                          "frac": 5.03125 * n / (r_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}},
+            "clocks": clocks.summary(),
+            "cpu_baseline": {"value": 1.0 / per_el, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": "oracle AdamW (float64) + MXFP8 requant on 262144 elements, scaled by elements",
+                             "sample_wall_s": time.perf_counter() - t0}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -712,6 +910,8 @@ def main():
     ap.add_argument("--skip-adamw", action="store_true")
     ap.add_argument("--skip-extra", action="store_true", help="skip the 32x32 / relayout / reduce-scatter timings")
     ap.add_argument("--graph", action="store_true", help="also time the fused step replayed from a CUDA graph")
+    ap.add_argument("--skip-configs", action="store_true",
+                    help="skip the per-class Newton-Schulz table and the other workloads (N = 1 only)")
     args = ap.parse_args()
     cfg = workloads.get(args.workload)
     if cfg.optimizer != "muon":

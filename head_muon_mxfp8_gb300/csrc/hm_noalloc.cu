@@ -1,11 +1,10 @@
 // Newton-Schulz of one update unit with no device allocation at all.
 //
-// For callers that cannot call cudaMalloc: code running while a stream is
-// being captured into a CUDA graph (an allocation there either fails or
-// synchronises), code inside a framework that has already handed all device
-// memory to its own caching allocator, and latency-critical paths that must
-// not take the driver's allocation lock or an implicit device
-// synchronisation.  The caller passes u and v; every intermediate (X,
+// For callers that cannot call cudaMalloc: code inside a framework that has
+// already handed all device memory to its own caching allocator (an
+// allocation of its own would fail or fragment that pool), and
+// latency-critical paths that must not take the driver's allocation lock or
+// an implicit device synchronisation.  The caller passes u and v; every intermediate (X,
 // A, B, the norm partials and the unit descriptor) lives in one file-scope
 // __device__ array of fixed size, which every GPU that loads the library
 // holds until the process exits.

@@ -293,9 +293,9 @@ hm_status mxfp8_requant_packed(const float* w, uint8_t* q, uint8_t* scales,
 /* ------------------------------------------------------------------------ */
 /* Newton-Schulz of one unit without any device allocation.  The paper has no
  * counterpart: this entry point exists for callers that cannot call
- * cudaMalloc -- code that runs while a stream is being captured into a CUDA
- * graph, code inside a framework whose caching allocator already owns all
- * device memory, and latency-critical paths that must not take the driver's
+ * cudaMalloc -- code inside a framework whose caching allocator already owns
+ * all device memory (a cudaMalloc of its own would fail or fragment the
+ * pool), and latency-critical paths that must not take the driver's
  * allocation lock or risk the implicit synchronisation an allocation brings.
  *
  * u: device, rows x cols bf16 bit patterns, row-major, 16-byte aligned; v:

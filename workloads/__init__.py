@@ -211,6 +211,19 @@ def scaled_muon(name: str, shapes: List[Tuple[int, int, Optional[int]]], so: int
     return Config(name, "test config", "muon", b.members, b.units, so=so, sw=sw, sg=sg)
 
 
+def class_subset(cfg: Config, m: int, n: int) -> Config:
+    """The members of cfg whose update units have shape class (min, max) =
+    (m, n), as a config of their own with the same rank degrees (for timing
+    one Newton-Schulz shape class alone)."""
+    b = _ListBuilder()
+    for mem in cfg.members:
+        us = [u for u in cfg.units if u.member == cfg.members.index(mem)]
+        if us and (min(us[0].rows, us[0].cols), max(us[0].rows, us[0].cols)) == (m, n):
+            b.add(mem.name, mem.rows, mem.cols, unit_rows=None if len(us) == 1 else us[0].rows)
+    return Config(f"{cfg.name}_class_{m}x{n}", f"the {m}x{n} units of {cfg.name}", "muon", b.members, b.units,
+                  so=cfg.so, sw=cfg.sw, sg=cfg.sg)
+
+
 CONFIGS = {
     "tiny": tiny,
     "flat_adamw": flat_adamw,
