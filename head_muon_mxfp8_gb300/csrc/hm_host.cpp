@@ -832,6 +832,37 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
                 hm::launch_ns_norm(c, ws, hp->eps, s) != cudaSuccess)
                 return HM_ERR_CUDA;
             const float* inv = reinterpret_cast<const float*>(ws + c.inv_off);
+            if (c.mp == 128) {
+                // Gram size 128 (the per-head units): every product of every
+                // iteration in one persistent kernel, X read once and written once
+                // per iteration, A and B kept on chip
+                hm::SmallNsParams sp{};
+                hm::GemmParams& g = sp.g;
+                g.ns_units = units_dev; g.v_root = b->v; g.v_stage = v_stage;
+                g.m_real = c.m; g.n_real = c.n;
+                g.err = hm::device_error_word();
+                g.inject_no_ready = inject ? 1 : 0;
+                inject = false;
+                g.unit_scale = inv;
+                if (epi_update) {
+                    g.fuse_update = 1;
+                    g.decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
+                    g.has_decay = hp->weight_decay != 0.f;
+                    g.frags = reinterpret_cast<const NsFrag*>(ws + p->off_nsf);
+                    g.w = b->w;
+                    g.q = b->q;
+                    g.s = b->s;
+                }
+                sp.units = c.n_units;
+                sp.np = c.np;
+                sp.steps = hp->ns_steps;
+                sp.reverse = 1;
+                sp.a = hp->ns_a;
+                sp.b = hp->ns_b;
+                sp.c = hp->ns_c;
+                if (hm::launch_ns_small(mp.x_a[0], mp.x_a[1], sp, s) != cudaSuccess) return HM_ERR_CUDA;
+                continue;
+            }
             auto bf = [&](size_t off) { return reinterpret_cast<uint16_t*>(ws + off); };
             int cur = 0;
             for (int it = 0; it < hp->ns_steps; ++it) {

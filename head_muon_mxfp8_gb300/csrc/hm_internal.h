@@ -125,6 +125,20 @@ struct GemmParams {
     uint8_t* s;
 };
 
+// Whole Newton-Schulz of a class whose Gram size mp is 128 in one persistent
+// kernel (every product of every iteration; X read once and written once per
+// iteration).  g carries the last product's epilogue fields (ns_units,
+// v_root, v_stage, m_real, n_real, fuse_update and its w, q, s, frags, decay),
+// err, inject_no_ready and unit_scale (1 / (||u|| + eps) per unit).
+struct SmallNsParams {
+    GemmParams g;
+    int32_t units;    // units of the class
+    int32_t np;       // padded row length of X (multiple of 64)
+    int32_t steps;    // Newton-Schulz iterations
+    int32_t reverse;  // alternate the tile order of consecutive passes over X
+    float a, b, c;
+};
+
 // chain geometry the device needs: z1 edges and the segment base of every chunk
 constexpr int kMaxChainRanks = 256;
 struct ChainArgs {
@@ -214,6 +228,10 @@ cudaError_t launch_ns_norm(const NsClassDev& c, char* ws, float eps, cudaStream_
 // b_mn: the B operand is MN-major (its map has 64 x 64 boxes, N innermost)
 cudaError_t launch_ns_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p,
                            int bn, int b_mn, cudaStream_t st);
+// The whole Newton-Schulz of a class with mp = 128, after the prepare pass and
+// the norm: x0 and x1 map the two X buffers [units][128][np] with 128-row x
+// 64-column boxes; X0 is in buffer 0.
+cudaError_t launch_ns_small(const CUtensorMap& x0, const CUtensorMap& x1, const SmallNsParams& p, cudaStream_t st);
 // CTA-pair (cta_group::2) variant: 256 x 256 tiles, M a multiple of 128; both
 // operand maps use 128-row boxes (64 x 64 boxes for an MN-major B)
 cudaError_t launch_ns_gemm_pair(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p, int b_mn,

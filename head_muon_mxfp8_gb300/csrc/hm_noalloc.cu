@@ -10,8 +10,9 @@
 // holds until the process exits.
 //
 // The computation is the same as the Newton-Schulz stage of
-// muon_update_units: the same norm, prepare and tcgen05 GEMM kernels, on the
-// built-in scratch instead of a caller workspace.
+// muon_update_units for a unit whose smaller side is at most 128: the same
+// prepare and norm kernels and the same one-launch tcgen05 Newton-Schulz
+// kernel, on the built-in scratch instead of a caller workspace.
 #include "hm.h"
 #include "hm_internal.h"
 
@@ -23,16 +24,13 @@ constexpr int kMaxM = HM_NOALLOC_MAX_MIN_DIM;   // padded Gram size of the scrat
 constexpr int kMaxN = HM_NOALLOC_MAX_MAX_DIM;
 constexpr size_t kSlot = 1024;
 constexpr size_t kXBytes = static_cast<size_t>(kMaxM) * kMaxN * 2;
-constexpr size_t kABytes = static_cast<size_t>(kMaxM) * kMaxM * 2;
 // one norm partial per 64 x 64 tile of X
 constexpr size_t kPartsBytes = (static_cast<size_t>(kMaxM / 64) * (kMaxN / 64) * 4 + kSlot - 1) / kSlot * kSlot;
-// layout: unit descriptor | X0 | X1 | A | B | partials | 1/norm
+// layout: unit descriptor | X0 | X1 | partials | 1/norm  (A and B stay on chip)
 constexpr size_t kOffUnit = 0;
 constexpr size_t kOffX0 = kSlot;
 constexpr size_t kOffX1 = kOffX0 + kXBytes;
-constexpr size_t kOffA = kOffX1 + kXBytes;
-constexpr size_t kOffB = kOffA + kABytes;
-constexpr size_t kOffParts = kOffB + kABytes;
+constexpr size_t kOffParts = kOffX1 + kXBytes;
 constexpr size_t kOffInv = kOffParts + kPartsBytes;
 constexpr size_t kScratchBytes = kOffInv + kSlot;
 static_assert(kScratchBytes == HM_NOALLOC_SCRATCH_BYTES, "scratch size stated in hm.h");
@@ -126,21 +124,13 @@ extern "C" hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int3
     c.parts = (c.np / 64) * (c.mp / 64);
     c.x_off[0] = kOffX0;
     c.x_off[1] = kOffX1;
-    c.a_off = kOffA;
-    c.b_off = kOffB;
     c.part_off = kOffParts;
     c.inv_off = kOffInv;
     hm::NsUnit* unit_dev = reinterpret_cast<hm::NsUnit*>(ws + kOffUnit);
 
-    CUtensorMap x_map[2], x_mn[2], a_map, b_map;
-    const int bn3 = c.np >= 256 ? 256 : 128;
+    CUtensorMap x_map[2];
     bool ok = true;
-    for (int b = 0; b < 2; ++b) {
-        ok = ok && map_bf16(&x_map[b], ws + c.x_off[b], c.np, c.mp, 128);
-        ok = ok && map_bf16(&x_mn[b], ws + c.x_off[b], c.np, c.mp, 64);
-    }
-    ok = ok && map_bf16(&a_map, ws + c.a_off, c.mp, c.mp, 128);
-    ok = ok && map_bf16(&b_map, ws + c.b_off, c.mp, c.mp, 128);
+    for (int b = 0; b < 2; ++b) ok = ok && map_bf16(&x_map[b], ws + c.x_off[b], c.np, c.mp, 128);
     if (!ok) return HM_ERR_CUDA;
 
     hm::note_launch();
@@ -149,38 +139,22 @@ extern "C" hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int3
     if (hm::launch_ns_prepare(c, unit_dev, u, nullptr, ws, st) != cudaSuccess ||
         hm::launch_ns_norm(c, ws, hp->eps, st) != cudaSuccess)
         return HM_ERR_CUDA;
-    const float* inv = reinterpret_cast<const float*>(ws + c.inv_off);
-    auto bf = [&](size_t off) { return reinterpret_cast<uint16_t*>(ws + off); };
-    int cur = 0;
-    for (int it = 0; it < hp->ns_steps; ++it) {
-        hm::GemmParams g1{};
-        g1.M = c.mp; g1.N = c.mp; g1.K = c.np; g1.units = 1;
-        g1.epi = hm::kEpiGram; g1.alpha = 1.f; g1.beta = 0.f;
-        g1.out = bf(c.a_off); g1.out_us = static_cast<int64_t>(c.mp) * c.mp; g1.ld_out = c.mp;
-        g1.err = hm::device_error_word();
-        g1.unit_scale = it == 0 ? inv : nullptr;  // X0 is u itself: A = s^2 u u^T
-        if (hm::launch_ns_gemm(x_map[cur], x_map[cur], g1, 128, 0, st) != cudaSuccess) return HM_ERR_CUDA;
-
-        hm::GemmParams g2 = g1;
-        g2.unit_scale = nullptr;
-        g2.K = c.mp;
-        g2.epi = hm::kEpiPoly; g2.alpha = hp->ns_c; g2.beta = hp->ns_b;
-        g2.add = bf(c.a_off); g2.add_us = g1.out_us; g2.ld_add = c.mp;
-        g2.out = bf(c.b_off);
-        if (hm::launch_ns_gemm(a_map, a_map, g2, 128, 0, st) != cudaSuccess) return HM_ERR_CUDA;
-
-        const bool last = it + 1 == hp->ns_steps;
-        hm::GemmParams g3{};
-        g3.M = c.mp; g3.N = c.np; g3.K = c.mp; g3.units = 1;
-        g3.epi = last ? hm::kEpiFinal : hm::kEpiUpdate; g3.alpha = 1.f; g3.beta = hp->ns_a;
-        g3.add = bf(c.x_off[cur]); g3.add_us = static_cast<int64_t>(c.mp) * c.np; g3.ld_add = c.np;
-        g3.out = bf(c.x_off[cur ^ 1]); g3.out_us = g3.add_us; g3.ld_out = c.np;
-        g3.ns_units = unit_dev; g3.v_root = v; g3.v_stage = nullptr;
-        g3.m_real = m; g3.n_real = n;
-        g3.err = g1.err;
-        g3.unit_scale = it == 0 ? inv : nullptr;  // X1 = s (a u + B u)
-        if (hm::launch_ns_gemm(b_map, x_mn[cur], g3, bn3, 1, st) != cudaSuccess) return HM_ERR_CUDA;
-        cur ^= 1;
-    }
+    // every product of every iteration in one kernel (the kernel
+    // muon_update_units runs for Gram size 128), on the built-in X buffers
+    hm::SmallNsParams sp{};
+    sp.g.ns_units = unit_dev;
+    sp.g.v_root = v;
+    sp.g.m_real = m;
+    sp.g.n_real = n;
+    sp.g.err = hm::device_error_word();
+    sp.g.unit_scale = reinterpret_cast<const float*>(ws + c.inv_off);
+    sp.units = 1;
+    sp.np = c.np;
+    sp.steps = hp->ns_steps;
+    sp.reverse = 1;
+    sp.a = hp->ns_a;
+    sp.b = hp->ns_b;
+    sp.c = hp->ns_c;
+    if (hm::launch_ns_small(x_map[0], x_map[1], sp, st) != cudaSuccess) return HM_ERR_CUDA;
     return HM_OK;
 }

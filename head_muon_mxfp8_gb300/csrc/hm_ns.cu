@@ -450,45 +450,38 @@ __device__ __forceinline__ void stage_add_addend(const GemmParams& p, float* sta
     }
 }
 
-// Last product with the update folded in (units flagged kNsEpiUpdate): the
-// chunk's 32 x 32 values of v = aX + BX (fp32, in the warp's swizzled staging
-// tile) never reach memory.  Each 1 x 32 MX block of the unit's w that the
-// chunk covers -- a row of the chunk, or a column when the unit is stored
-// transposed (X = u^T) -- is read from the root, updated as f2 does it
-// (w*decay - step*v, or w - step*v, each product and the difference rounded
-// once) and quantized as G does it, so w, q and s come out bit-identical to
-// the pass through v.  Four lanes own one block, 8 elements each (lane l:
-// block l/4 + 8s, elements 8(l%4)..+7); the loads of all four blocks go first.
-// (Issuing them before the aX addend is folded in, or a tile ahead as L2
-// prefetches, measured no faster.)
-//
-// base1: root offset minus unit offset of a unit with one fragment (a local
-// unit), read once per tile; -1 = look the fragment up per block.
-__device__ __forceinline__ void final_update_chunk(const GemmParams& p, const NsUnit& nu, int64_t base1,
-                                                   const float* stage, int i0, int j0) {
+// Root offsets of the four 1 x 32 blocks of w this lane works on in the chunk
+// (rows i0.., columns j0.. of X): lane l takes block l/4 + 8s, elements
+// 8(l%4)..+7; -1 for a row of w beyond the unit.  False when the chunk lies in
+// X's zero padding (warp-uniform).
+__device__ __forceinline__ bool chunk_w_blocks(const GemmParams& p, const NsUnit& nu, int64_t base1, int i0, int j0,
+                                               int64_t (&dst)[4]) {
     const int lane = threadIdx.x & 31;
     const bool tr = nu.flags & kNsTransposed;
     const int kw = tr ? p.m_real : p.n_real;      // length of a row of w (the MX K)
     const int rows_w = tr ? p.n_real : p.m_real;  // rows of w
     const int rw0 = tr ? j0 : i0;                  // w row of the chunk's block 0
     const int cw0 = tr ? i0 : j0;                  // w column of every block's first element
-    if (cw0 >= kw) return;                         // padding of X (warp-uniform)
-    const int cq = (lane & 3) * 8;
-    int64_t dst[4];
-    float4 w0[4], w1[4];
+    if (cw0 >= kw) return false;                   // padding of X
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const int rw = rw0 + (lane >> 2) + 8 * s;
-        w0[s] = w1[s] = make_float4(0.f, 0.f, 0.f, 0.f);
         dst[s] = -1;
         if (rw >= rows_w) continue;
         // the unit's fragment that holds this block (32-aligned: the whole block)
         const int64_t e = static_cast<int64_t>(rw) * kw + cw0;
         dst[s] = base1 >= 0 ? base1 + e : unit_root_offset(p, nu, e);
-        const float4* wp = reinterpret_cast<const float4*>(p.w + dst[s] + cq);
-        w0[s] = __ldcs(wp);
-        w1[s] = __ldcs(wp + 1);
     }
+    return true;
+}
+
+// f2 and G of the chunk's w blocks from their loaded values (w0, w1: this
+// lane's 8 elements of block s) and the staged v.
+__device__ __forceinline__ void update_w_blocks(const GemmParams& p, const NsUnit& nu, const float* stage,
+                                                const int64_t (&dst)[4], const float4 (&w0)[4], const float4 (&w1)[4]) {
+    const int lane = threadIdx.x & 31;
+    const bool tr = nu.flags & kNsTransposed;
+    const int cq = (lane & 3) * 8;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const int kk = (lane >> 2) + 8 * s;
@@ -525,6 +518,84 @@ __device__ __forceinline__ void final_update_chunk(const GemmParams& p, const Ns
         const uint32_t c67 = cvt_e4m3x2(x[6] * sc, x[7] * sc);
         __stcs(reinterpret_cast<uint2*>(p.q + dst[s] + cq), make_uint2(c01 | (c23 << 16), c45 | (c67 << 16)));
         if ((lane & 3) == 0) p.s[dst[s] >> 5] = static_cast<uint8_t>(ex + 127);
+    }
+}
+
+// Last product with the update folded in (units flagged kNsEpiUpdate): the
+// chunk's 32 x 32 values of v = aX + BX (fp32, in the warp's swizzled staging
+// tile) never reach memory.  Each 1 x 32 MX block of the unit's w that the
+// chunk covers -- a row of the chunk, or a column when the unit is stored
+// transposed (X = u^T) -- is read from the root, updated as f2 does it
+// (w*decay - step*v, or w - step*v, each product and the difference rounded
+// once) and quantized as G does it, so w, q and s come out bit-identical to
+// the pass through v.  Four lanes own one block, 8 elements each (lane l:
+// block l/4 + 8s, elements 8(l%4)..+7); the loads of all four blocks go first.
+// (Issuing them before the aX addend is folded in, or a tile ahead as L2
+// prefetches, measured no faster.)
+//
+// base1: root offset minus unit offset of a unit with one fragment (a local
+// unit), read once per tile; -1 = look the fragment up per block.
+__device__ __forceinline__ void final_update_chunk(const GemmParams& p, const NsUnit& nu, int64_t base1,
+                                                   const float* stage, int i0, int j0) {
+    int64_t dst[4];
+    if (!chunk_w_blocks(p, nu, base1, i0, j0, dst)) return;
+    const int cq = (threadIdx.x & 3) * 8;
+    float4 w0[4], w1[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        w0[s] = w1[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (dst[s] < 0) continue;
+        const float4* wp = reinterpret_cast<const float4*>(p.w + dst[s] + cq);
+        w0[s] = __ldcs(wp);
+        w1[s] = __ldcs(wp + 1);
+    }
+    update_w_blocks(p, nu, stage, dst, w0, w1);
+}
+
+// The last product's 32 x 32 chunk (rows i0.., columns j0.. of X; this lane's
+// row is i), parked in the warp's staging tile as fp32 values of aX + BX:
+// f2 and G of the unit straight from the staging (fuse), or v written to the
+// unit's own v location.
+__device__ __forceinline__ void store_final_chunk(const GemmParams& p, const NsUnit& nu, bool fuse, int64_t base1,
+                                                  const float* stage, int i, int i0, int j0) {
+    if (fuse) {
+        final_update_chunk(p, nu, base1, stage, i0, j0);
+        return;
+    }
+    const int lane = threadIdx.x & 31;
+    float* dst = ((nu.flags & kNsVStaged) ? p.v_stage : p.v_root) + nu.v_off;
+    if (nu.flags & kNsTransposed) {
+        // v is X^T: for each k the 32 lanes write 32 consecutive floats
+        // of v's row j0 + k
+        if (i < p.m_real) {
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 y = stage4_ld(stage, lane, c4);
+                const float yk[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (j0 + 4 * c4 + e < p.n_real)
+                        __stcs(dst + static_cast<int64_t>(j0 + 4 * c4 + e) * p.m_real + i, yk[e]);
+            }
+        }
+    } else if (j0 + 32 <= p.n_real && (p.n_real & 3) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+        // row-major v: 8 lanes per row, 16 bytes each, so every store covers
+        // 4 rows x 128 contiguous bytes; streaming stores, since v is read
+        // back only by f2 after the whole Newton-Schulz stage
+        const int c4 = lane & 7;
+#pragma unroll 1
+        for (int s2 = 0; s2 < 8; ++s2) {
+            const int r2 = s2 * 4 + (lane >> 3);
+            if (i0 + r2 < p.m_real)
+                __stcs(reinterpret_cast<float4*>(dst + static_cast<int64_t>(i0 + r2) * p.n_real + j0 + 4 * c4),
+                       stage4_ld(stage, r2, c4));
+        }
+    } else if (j0 + lane < p.n_real) {
+        // ragged or unaligned rows: one 4-byte store per lane, 128 bytes of one row per store
+#pragma unroll 4
+        for (int r2 = 0; r2 < 32; ++r2)
+            if (i0 + r2 < p.m_real)
+                dst[static_cast<int64_t>(i0 + r2) * p.n_real + j0 + lane] = stage_at(stage, r2, lane);
     }
 }
 
@@ -608,46 +679,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int u, int i_
             // or f2 and G of the unit straight from the staging
             stage_add_addend(p, stage, a, usc);
             __syncwarp();
-            if (fuse) {
-                final_update_chunk(p, nu, base1, stage, i0, j0);
-                __syncwarp();
-                continue;
-            }
-            float* dst = ((nu.flags & kNsVStaged) ? p.v_stage : p.v_root) + nu.v_off;
-            if (nu.flags & kNsTransposed) {
-                // v is X^T: for each k the 32 lanes write 32 consecutive floats
-                // of v's row j0 + k
-                if (i < p.m_real) {
-#pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const float4 y = *st4(lane, c4);
-                        const float yk[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (j0 + 4 * c4 + e < p.n_real)
-                                __stcs(dst + static_cast<int64_t>(j0 + 4 * c4 + e) * p.m_real + i, yk[e]);
-                    }
-                }
-            } else if (j0 + 32 <= p.n_real && (p.n_real & 3) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
-                // row-major v: 8 lanes per row, 16 bytes each, so every store covers
-                // 4 rows x 128 contiguous bytes; streaming stores, since v is read
-                // back only by f2 after the whole Newton-Schulz stage
-                const int c4 = lane & 7;
-#pragma unroll 1
-                for (int s2 = 0; s2 < 8; ++s2) {
-                    const int r2 = s2 * 4 + (lane >> 3);
-                    if (i0 + r2 < p.m_real)
-                        __stcs(reinterpret_cast<float4*>(dst + static_cast<int64_t>(i0 + r2) * p.n_real + j0 + 4 * c4),
-                               *st4(r2, c4));
-                }
-            } else if (j0 + lane < p.n_real) {
-                // ragged or unaligned rows: one 4-byte store per lane, 128 bytes of one row per store
-#pragma unroll 4
-                for (int r2 = 0; r2 < 32; ++r2)
-                    if (i0 + r2 < p.m_real)
-                        dst[static_cast<int64_t>(i0 + r2) * p.n_real + j0 + lane] =
-                            stage_at(stage, r2, lane);
-            }
+            store_final_chunk(p, nu, fuse, base1, stage, i, i0, j0);
             __syncwarp();
             continue;
         }
@@ -1132,6 +1164,535 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Whole Newton-Schulz of a class whose Gram size is 128 (m <= 128: the
+// per-head units) in one persistent kernel.  A CTA takes whole units (unit
+// blockIdx.x, then + gridDim.x, ...) and keeps all but X on chip: A and B
+// (128 x 128) live in TMEM and shared memory while X streams through a ring
+// of 128-row x 64-column tiles.  Per unit:
+//   Gram pass:   A = X0 X0^T, accumulated over X0's tiles;
+//   iteration:   B = bA + cAA (A and B rounded to bf16 in shared memory),
+//                then one pass over X's tiles: X'_j = aX_j + B X_j and --
+//                except in the last iteration -- A' += X'_j X'_j^T, read
+//                from the bf16 X'_j the epilogue has just written to shared
+//                memory, which a TMA store also sends to the other X buffer
+//                for the next pass.  The last iteration writes v, or applies
+//                f2 and G, instead of storing X'.
+// So X is read once per iteration and written once, where the three-launch
+// form reads it in X X^T, again in B X, and writes X'.  Consecutive passes
+// run in opposite tile orders, so each starts on the tiles the previous one
+// touched last, which are still in the L2.  The element-wise arithmetic of
+// every product is that of the three-launch epilogues; only the order in
+// which A's fp32 sums are accumulated over the tiles differs.
+// Roles (11 warps): warp 0 issues the TMA loads, warp 1 allocates TMEM and
+// issues the MMAs, warp 2 the TMA stores of X', warps 3-10 run the
+// epilogues (two per TMEM lane quadrant; for a 64-column tile each drains
+// 32 columns, for A and B each 64).
+// TMEM: A [0, 128), AA [128, 256), four 64-column B X accumulators [256, 512).
+// Every wait is bounded, as in the GEMM kernels.
+// ---------------------------------------------------------------------------
+constexpr int kSmallThreads = 352;
+constexpr int kSmallRing = 5;                // X tiles in flight
+constexpr int kSmallNB = 4;                  // B X accumulators
+constexpr int kSmallTile = 128 * 64 * 2;     // a 128 x 64 bf16 tile (16 KB)
+struct SmallCfg {
+    static constexpr int RING_OFF = 0;
+    static constexpr int AS_OFF = RING_OFF + kSmallRing * kSmallTile;  // A, bf16: two [128][64] K atoms
+    static constexpr int BS_OFF = AS_OFF + 2 * kSmallTile;              // B, bf16: the same layout
+    static constexpr int XO_OFF = BS_OFF + 2 * kSmallTile;              // X' tiles, two buffers
+    static constexpr int ST_OFF = XO_OFF + 2 * kSmallTile;              // per epilogue warp a 32 x 32 fp32 tile
+    static constexpr int BAR_OFF = ST_OFF + kEpiWarps * 32 * 32 * 4;
+    static constexpr int SMEM = BAR_OFF + 512 + 1024;
+    // kind::f16, D fp32, A and B bf16: M = N = 128 with both operands K-major
+    // (A X X^T and A A); M = 128, N = 64 with B MN-major (B X)
+    static constexpr uint32_t IDESC_G = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+    static constexpr uint32_t IDESC_BX =
+        (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+};
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// 16-byte chunk c (8 bf16) of row r of a [128][64] bf16 tile written with the
+// 128-byte swizzle (the layout of the TMA boxes and of the MMA operands)
+__device__ __forceinline__ uint32_t tile_chunk(int r, int c) {
+    return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// The last product with f2 and G folded in reads w one chunk ahead: this
+// lane's 8 elements of each of the chunk's four w blocks are copied
+// asynchronously into the warp's 4 KB buffer (float4 (2s + half) * 32 + lane,
+// so the read-back is conflict-free), then consumed a tile later.
+__device__ __forceinline__ void prefetch_w_chunk(const GemmParams& p, const NsUnit& nu, int64_t base1, int i0, int j0,
+                                                 uint32_t buf) {
+    int64_t dst[4];
+    if (!chunk_w_blocks(p, nu, base1, i0, j0, dst)) return;
+    const int lane = threadIdx.x & 31;
+    const int cq = (lane & 3) * 8;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        if (dst[s] < 0) continue;
+        const float* src = p.w + dst[s] + cq;
+        cp_async16(buf + ((2 * s) * 32 + lane) * 16, src);
+        cp_async16(buf + ((2 * s + 1) * 32 + lane) * 16, src + 4);
+    }
+}
+__device__ __forceinline__ void final_update_chunk_buf(const GemmParams& p, const NsUnit& nu, int64_t base1,
+                                                       const float* stage, int i0, int j0, const float4* buf) {
+    int64_t dst[4];
+    if (!chunk_w_blocks(p, nu, base1, i0, j0, dst)) return;
+    const int lane = threadIdx.x & 31;
+    float4 w0[4], w1[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        w0[s] = w1[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (dst[s] < 0) continue;
+        w0[s] = buf[(2 * s) * 32 + lane];
+        w1[s] = buf[(2 * s + 1) * 32 + lane];
+    }
+    update_w_blocks(p, nu, stage, dst, w0, w1);
+}
+
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    ns_small_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant__ CUtensorMap tx1,
+                    const __grid_constant__ SmallNsParams sp) {
+    using C = SmallCfg;
+    const GemmParams& p = sp.g;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = smem + C::RING_OFF;
+    uint8_t* as = smem + C::AS_OFF;
+    uint8_t* bs = smem + C::BS_OFF;
+    uint8_t* xo = smem + C::XO_OFF;
+    float* stg = reinterpret_cast<float*>(smem + C::ST_OFF);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    uint64_t* x_full = bars;                   // ring slot loaded
+    uint64_t* x_emma = x_full + kSmallRing;    // slot released by the Gram MMA (Gram-pass tiles)
+    uint64_t* x_eepi = x_emma + kSmallRing;    // slot released by the epilogue (B X tiles: the aX addend)
+    uint64_t* d_full = x_eepi + kSmallRing;
+    uint64_t* d_empty = d_full + kSmallNB;
+    uint64_t* xo_full = d_empty + kSmallNB;    // X' tile written (for the Gram MMA and the store)
+    uint64_t* xo_free = xo_full + 2;           // its Gram MMA done
+    uint64_t* xs_done = xo_free + 2;           // its TMA store has read it
+    uint64_t* gram_full = xs_done + 2;         // A complete in TMEM
+    uint64_t* a_ready = gram_full + 1;         // A in shared memory
+    uint64_t* aa_full = a_ready + 1;           // AA complete in TMEM
+    uint64_t* b_ready = aa_full + 1;           // B in shared memory
+    uint64_t* st_done = b_ready + 1;           // an iteration's X' all in global memory
+    uint64_t* drain = st_done + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* bail = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSmallRing; ++s) {
+            mbar_init(smem_u32(&x_full[s]), 1);
+            mbar_init(smem_u32(&x_emma[s]), 1);
+            mbar_init(smem_u32(&x_eepi[s]), kEpiWarps);
+        }
+        for (int b = 0; b < kSmallNB; ++b) {
+            mbar_init(smem_u32(&d_full[b]), 1);
+            mbar_init(smem_u32(&d_empty[b]), kEpiWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&xo_full[b]), kEpiWarps);
+            mbar_init(smem_u32(&xo_free[b]), 1);
+            mbar_init(smem_u32(&xs_done[b]), 1);
+        }
+        mbar_init(smem_u32(gram_full), 1);
+        mbar_init(smem_u32(a_ready), kEpiWarps);
+        mbar_init(smem_u32(aa_full), 1);
+        mbar_init(smem_u32(b_ready), kEpiWarps);
+        mbar_init(smem_u32(st_done), 1);
+        mbar_init(smem_u32(drain), 1);
+        *bail = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int nt = sp.np / 64;  // tiles per pass
+    const int S = sp.steps;
+    // tile of step t of pass k (k = 0: the Gram pass over X0; k = it + 1: iteration it)
+    auto tile_of = [&](int k, int t) { return (sp.reverse && (k & 1)) ? nt - 1 - t : t; };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t kind = 0;              // bit s: slot s last held a B X tile (released by the epilogue)
+            uint32_t par_m = 0, par_e = 0;  // bit s: parity of the next release of slot s, per releaser
+            uint32_t armed = 0, armed_par = 0;
+            int pos = 0, sd = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < sp.units && ok; u += gridDim.x) {
+                for (int k = 0; k <= S && ok; ++k) {
+                    const CUtensorMap* map = (k == 0 || ((k - 1) & 1) == 0) ? &tx0 : &tx1;
+                    if (k >= 2) {
+                        // X_{k-1} is the previous iteration's X': wait until all of it is stored
+                        if (!mbar_wait(smem_u32(st_done), sd & 1, p.err, bail)) { ok = false; break; }
+                        ++sd;
+                        fence_async_global();
+                    }
+                    for (int t = 0; t < nt; ++t) {
+                        const int s = pos % kSmallRing;
+                        if (pos >= kSmallRing) {
+                            const bool e = (kind >> s) & 1u;
+                            uint32_t& par = e ? par_e : par_m;
+                            if (!mbar_wait(smem_u32(e ? &x_eepi[s] : &x_emma[s]), (par >> s) & 1u, p.err, bail)) {
+                                ok = false;
+                                break;
+                            }
+                            par ^= 1u << s;
+                        }
+                        kind = (kind & ~(1u << s)) | ((k > 0 ? 1u : 0u) << s);
+                        const uint32_t fb = smem_u32(&x_full[s]);
+                        mbar_arrive_expect_tx(fb, kSmallTile);
+                        tma_load_3d(smem_u32(ring + s * kSmallTile), map, fb, tile_of(k, t) * 64, 0, u);
+                        armed |= 1u << s;
+                        armed_par = (armed_par & ~(1u << s)) | ((static_cast<uint32_t>(pos / kSmallRing) & 1u) << s);
+                        ++pos;
+                    }
+                }
+            }
+            // wait for this CTA's own copies still in flight
+            for (int s = 0; s < kSmallRing; ++s)
+                if (armed & (1u << s)) mbar_wait(smem_u32(&x_full[s]), (armed_par >> s) & 1u, p.err, bail, false);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t t_a = tmem, t_aa = tmem + 128, t_d = tmem + 256;
+            int pos = 0, dpos = 0, xg = 0;
+            uint32_t ar = 0, br = 0;
+            bool ok = true, first = true;
+            // A (+)= T T^T for a 128 x 64 tile T in shared memory
+            auto gram_on = [&](uint32_t saddr, bool acc0) {
+                const uint64_t d = desc_sw128(saddr);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) umma_bf16(t_a, d + 2 * kk, d + 2 * kk, C::IDESC_G, (acc0 || kk) ? 1u : 0u);
+            };
+            for (int u = blockIdx.x; u < sp.units && ok; u += gridDim.x) {
+                for (int t = 0; t < nt; ++t) {
+                    const int s = pos % kSmallRing;
+                    if (!mbar_wait(smem_u32(&x_full[s]), (pos / kSmallRing) & 1, p.err, bail)) { ok = false; break; }
+                    tc_fence_after();
+                    gram_on(smem_u32(ring + s * kSmallTile), t > 0);
+                    umma_commit(smem_u32(&x_emma[s]));
+                    ++pos;
+                }
+                if (!ok) break;
+                if (!(first && p.inject_no_ready)) umma_commit(smem_u32(gram_full));
+                first = false;
+                for (int it = 0; it < S && ok; ++it) {
+                    if (!mbar_wait(smem_u32(a_ready), ar & 1u, p.err, bail)) { ok = false; break; }
+                    ++ar;
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(as);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t d = desc_sw128(a0 + (kk >> 2) * kSmallTile) + 2 * (kk & 3);
+                        umma_bf16(t_aa, d, d, C::IDESC_G, kk ? 1u : 0u);
+                    }
+                    umma_commit(smem_u32(aa_full));
+                    if (!mbar_wait(smem_u32(b_ready), br & 1u, p.err, bail)) { ok = false; break; }
+                    ++br;
+                    tc_fence_after();
+                    const bool last = it + 1 == S;
+                    const uint32_t b0 = smem_u32(bs);
+                    for (int t = 0; t < nt; ++t) {
+                        const int s = pos % kSmallRing;
+                        const int db = dpos % kSmallNB;
+                        if (!mbar_wait(smem_u32(&x_full[s]), (pos / kSmallRing) & 1, p.err, bail)) { ok = false; break; }
+                        if (dpos >= kSmallNB &&
+                            !mbar_wait(smem_u32(&d_empty[db]), ((dpos / kSmallNB) - 1) & 1, p.err, bail)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t xd = desc_mn_sw128(smem_u32(ring + s * kSmallTile));
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_bf16(t_d + 64 * db, desc_sw128(b0 + (kk >> 2) * kSmallTile) + 2 * (kk & 3),
+                                      xd + 128 * kk, C::IDESC_BX, kk ? 1u : 0u);
+                        umma_commit(smem_u32(&d_full[db]));
+                        ++dpos;
+                        ++pos;
+                        if (!last && t >= 1) {
+                            // the next A from the previous tile's X' (one tile behind, so the
+                            // B X of this tile is issued before waiting for that epilogue)
+                            const int b = xg & 1;
+                            if (!mbar_wait(smem_u32(&xo_full[b]), (xg >> 1) & 1, p.err, bail)) { ok = false; break; }
+                            tc_fence_after();
+                            gram_on(smem_u32(xo + b * kSmallTile), t > 1);
+                            umma_commit(smem_u32(&xo_free[b]));
+                            ++xg;
+                        }
+                    }
+                    if (!ok) break;
+                    if (!last) {
+                        const int b = xg & 1;
+                        if (!mbar_wait(smem_u32(&xo_full[b]), (xg >> 1) & 1, p.err, bail)) { ok = false; break; }
+                        tc_fence_after();
+                        gram_on(smem_u32(xo + b * kSmallTile), nt > 1);
+                        umma_commit(smem_u32(&xo_free[b]));
+                        ++xg;
+                        umma_commit(smem_u32(gram_full));
+                    }
+                }
+            }
+            // every MMA this thread issued has completed before TMEM is freed
+            umma_commit(smem_u32(drain));
+            mbar_wait(smem_u32(drain), 0, p.err, bail, false);
+        }
+    } else if (warp == 2) {
+        if (lane == 0) {
+            int xg = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < sp.units && ok; u += gridDim.x) {
+                for (int it = 0; it + 1 < S && ok; ++it) {
+                    const CUtensorMap* map = ((it + 1) & 1) ? &tx1 : &tx0;
+                    for (int t = 0; t < nt; ++t) {
+                        const int b = xg & 1;
+                        if (!mbar_wait(smem_u32(&xo_full[b]), (xg >> 1) & 1, p.err, bail)) { ok = false; break; }
+                        tma_store_3d(map, smem_u32(xo + b * kSmallTile), tile_of(it + 1, t) * 64, 0, u);
+                        bulk_commit();
+                        bulk_wait_read_all();
+                        mbar_arrive(smem_u32(&xs_done[b]));
+                        ++xg;
+                    }
+                    if (!ok) break;
+                    bulk_wait_all();
+                    fence_async_global();
+                    mbar_arrive(smem_u32(st_done));
+                }
+            }
+            bulk_wait_all();
+        }
+    } else {
+        const int ew = warp - 3;         // epilogue warp 0..7
+        const int q = warp & 3;          // TMEM lane quadrant of this warp
+        const int h = ew >> 2;           // which half of a tile's (or of A's) columns
+        const int row = q * 32 + lane;   // row of A, B and X
+        float* stage = stg + ew * 1024;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        int pos = 0, dpos = 0, xg = 0;
+        uint32_t gf = 0, af = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < sp.units && ok; u += gridDim.x) {
+            pos += nt;  // the Gram pass's tiles are released by the MMA
+            const float usc = p.unit_scale ? p.unit_scale[u] : 1.f;
+            for (int it = 0; it < S && ok; ++it) {
+                const bool last = it + 1 == S;
+                // A = X X^T (s^2 u u^T in the first iteration), bf16, into shared memory
+                ok = mbar_wait(smem_u32(gram_full), gf & 1u, p.err, bail);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ++gf;
+                tc_fence_after();
+                const float alpha_t = it == 0 ? 1.f * (usc * usc) : 1.f;
+                {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tl + h * 64, r0);
+                    tmem_ld32(tl + h * 64 + 32, r1);
+                    tmem_ld_wait();
+                    tmem_ld_pin(r0);
+                    tmem_ld_pin(r1);
+                    uint8_t* dst = as + h * kSmallTile;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t* r = c < 4 ? r0 + 8 * c : r1 + 8 * (c - 4);
+                        *reinterpret_cast<uint4*>(dst + tile_chunk(row, c)) = make_uint4(
+                            bf16x2_bits(__uint_as_float(r[0]) * alpha_t, __uint_as_float(r[1]) * alpha_t),
+                            bf16x2_bits(__uint_as_float(r[2]) * alpha_t, __uint_as_float(r[3]) * alpha_t),
+                            bf16x2_bits(__uint_as_float(r[4]) * alpha_t, __uint_as_float(r[5]) * alpha_t),
+                            bf16x2_bits(__uint_as_float(r[6]) * alpha_t, __uint_as_float(r[7]) * alpha_t));
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(a_ready));
+                // B = bA + cAA, bf16, into shared memory
+                ok = mbar_wait(smem_u32(aa_full), af & 1u, p.err, bail);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ++af;
+                tc_fence_after();
+                {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tl + 128 + h * 64, r0);
+                    tmem_ld32(tl + 128 + h * 64 + 32, r1);
+                    tmem_ld_wait();
+                    tmem_ld_pin(r0);
+                    tmem_ld_pin(r1);
+                    const uint8_t* src = as + h * kSmallTile;
+                    uint8_t* dst = bs + h * kSmallTile;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t* r = c < 4 ? r0 + 8 * c : r1 + 8 * (c - 4);
+                        float a8[8], o[8];
+                        unpack_bf16x8(*reinterpret_cast<const uint4*>(src + tile_chunk(row, c)), a8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = fmaf(sp.b, a8[e], __uint_as_float(r[e]) * sp.c);
+                        *reinterpret_cast<uint4*>(dst + tile_chunk(row, c)) =
+                            make_uint4(bf16x2_bits(o[0], o[1]), bf16x2_bits(o[2], o[3]), bf16x2_bits(o[4], o[5]),
+                                       bf16x2_bits(o[6], o[7]));
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(b_ready));
+                // the last product's destination, once per unit
+                NsUnit nu{};
+                bool fuse = false;
+                int64_t base1 = -1;
+                // w buffers of the last pass: the 4 KB of A that this warp wrote (idle
+                // once B is formed) and a 4 KB block of the X' tiles, which the last
+                // pass does not store
+                uint8_t* wbuf[2] = {as + h * kSmallTile + q * 4096, xo + h * kSmallTile + q * 4096};
+                if (last) {
+                    nu = p.ns_units[u];
+                    fuse = p.fuse_update && (nu.flags & kNsEpiUpdate);
+                    if (fuse && nu.nfrag == 1) base1 = p.frags[nu.frag0].root_off - p.frags[nu.frag0].unit_off;
+                }
+                if (fuse) {
+                    // the X' tiles' last stores have read them
+                    if (xg >= 1) ok = mbar_wait(smem_u32(&xs_done[(xg - 1) & 1]), ((xg - 1) >> 1) & 1, p.err, bail);
+                    if (ok && xg >= 2) ok = mbar_wait(smem_u32(&xs_done[(xg - 2) & 1]), ((xg - 2) >> 1) & 1, p.err, bail);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    prefetch_w_chunk(p, nu, base1, q * 32, tile_of(S, 0) * 64 + h * 32, smem_u32(wbuf[0]));
+                    cp_async_commit();
+                }
+                // the pass over X: X' = a X + B X per tile
+                for (int t = 0; t < nt; ++t) {
+                    const int j = tile_of(it + 1, t);
+                    const int db = dpos % kSmallNB;
+                    if (fuse) {
+                        if (t + 1 < nt)
+                            prefetch_w_chunk(p, nu, base1, q * 32, tile_of(S, t + 1) * 64 + h * 32,
+                                             smem_u32(wbuf[(t + 1) & 1]));
+                        cp_async_commit();
+                    }
+                    ok = mbar_wait(smem_u32(&d_full[db]), (dpos / kSmallNB) & 1, p.err, bail);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                    uint32_t r[32];
+                    tmem_ld32(tl + 256 + db * 64 + h * 32, r);
+                    tmem_ld_wait();
+                    tmem_ld_pin(r);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&d_empty[db]));
+                    ++dpos;
+                    // this lane's row of the X tile (32 columns): the aX addend
+                    const int s = pos % kSmallRing;
+                    ok = mbar_wait(smem_u32(&x_full[s]), (pos / kSmallRing) & 1, p.err, bail);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    const uint8_t* xt = ring + s * kSmallTile;
+                    float y[32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float x8[8];
+                        unpack_bf16x8(*reinterpret_cast<const uint4*>(xt + tile_chunk(row, 4 * h + c)), x8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) y[8 * c + e] = fmaf(sp.a, x8[e], __uint_as_float(r[8 * c + e]));
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&x_eepi[s]));
+                    ++pos;
+                    if (it == 0) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) y[e] *= usc;
+                    }
+                    if (!last) {
+                        // bf16 X' into its shared tile, for the next A and the store
+                        const int b = xg & 1;
+                        if (xg >= 2) {
+                            ok = mbar_wait(smem_u32(&xo_free[b]), ((xg >> 1) - 1) & 1, p.err, bail) &&
+                                 mbar_wait(smem_u32(&xs_done[b]), ((xg >> 1) - 1) & 1, p.err, bail);
+                            ok = __all_sync(0xffffffffu, ok);
+                            if (!ok) break;
+                        }
+                        uint8_t* dst = xo + b * kSmallTile;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<uint4*>(dst + tile_chunk(row, 4 * h + c)) =
+                                make_uint4(bf16x2_bits(y[8 * c], y[8 * c + 1]), bf16x2_bits(y[8 * c + 2], y[8 * c + 3]),
+                                           bf16x2_bits(y[8 * c + 4], y[8 * c + 5]),
+                                           bf16x2_bits(y[8 * c + 6], y[8 * c + 7]));
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&xo_full[b]));
+                        ++xg;
+                    } else {
+                        // v = a X + B X: this lane's row into the warp's staging tile, then
+                        // v stored or f2 and G applied, as in the three-launch form
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4)
+                            *stage4(stage, lane, c4) = make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]);
+                        __syncwarp();
+                        if (fuse) {
+                            cp_async_wait_1();  // this tile's w (the next tile's may be in flight)
+                            final_update_chunk_buf(p, nu, base1, stage, q * 32, j * 64 + h * 32,
+                                                   reinterpret_cast<const float4*>(wbuf[t & 1]));
+                        } else {
+                            store_final_chunk(p, nu, fuse, base1, stage, row, q * 32, j * 64 + h * 32);
+                        }
+                        __syncwarp();
+                    }
+                }
+                if (fuse) cp_async_wait_all();
+            }
+        }
+        cp_async_wait_all();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+cudaError_t launch_small(const CUtensorMap& x0, const CUtensorMap& x1, const SmallNsParams& sp, cudaStream_t st) {
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SmallCfg::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    if (sp.units == 0) return cudaSuccess;
+    const int grid = sp.units < device_sm_count() ? sp.units : device_sm_count();
+    note_launch();
+    ns_small_kernel<<<grid, kSmallThreads, SmallCfg::SMEM, st>>>(x0, x1, sp);
+    return cudaGetLastError();
+}
+
 template <bool B_MN>
 cudaError_t launch_gemm_pair(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p0, cudaStream_t st) {
     using C = PairCfg<B_MN>;
@@ -1206,6 +1767,10 @@ cudaError_t launch_ns_norm(const NsClassDev& c, char* ws, float eps, cudaStream_
     ns_norm_final_kernel<<<c.n_units, kNormThreads, 0, st>>>(reinterpret_cast<const float*>(ws + c.part_off), c.parts,
                                                              reinterpret_cast<float*>(ws + c.inv_off), eps);
     return cudaGetLastError();
+}
+
+cudaError_t launch_ns_small(const CUtensorMap& x0, const CUtensorMap& x1, const SmallNsParams& p, cudaStream_t st) {
+    return launch_small(x0, x1, p, st);
 }
 
 cudaError_t launch_ns_gemm_pair(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p, int b_mn,

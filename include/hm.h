@@ -317,7 +317,7 @@ hm_status mxfp8_requant_packed(const float* w, uint8_t* q, uint8_t* scales,
  * race; serialise them.  Launches on `stream`; allocates nothing. */
 #define HM_NOALLOC_MAX_MIN_DIM 128
 #define HM_NOALLOC_MAX_MAX_DIM 8192
-#define HM_NOALLOC_SCRATCH_BYTES 4262912
+#define HM_NOALLOC_SCRATCH_BYTES 4197376
 hm_status newton_schulz_noalloc(const uint16_t* u, int32_t rows, int32_t cols, float* v,
                                 const hm_muon_hparams* hp, void* stream);
 

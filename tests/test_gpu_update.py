@@ -388,8 +388,9 @@ def test_empty_inputs_are_noops(hm, dev):
 @pytest.mark.parametrize("name,step", [("tiny", False), ("mixed", False), ("tiny", True), ("mixed", True)])
 def test_kernel_launch_count_of_one_fused_update(hm, dev, name, step):
     """One fused update launches f0 (with the gather), per shape class the
-    prepare pass (which also leaves the norm's partial sums), the norm and 3
-    products per Newton-Schulz iteration, then f2 with the requant -- which
+    prepare pass (which also leaves the norm's partial sums), the norm and
+    either one kernel for the whole iteration (Gram size 128) or 3 products
+    per Newton-Schulz iteration, then f2 with the requant -- which
     HM_STAGE_STEP drops when the last products update every unit themselves:
     the library's launch counter reports exactly that many kernels."""
     cfg = workloads.get(name)
@@ -404,7 +405,10 @@ def test_kernel_launch_count_of_one_fused_update(hm, dev, name, step):
     torch.cuda.synchronize()
     assert hm.hm_device_error() == 0
     rest = not step or not all(_epilogue_updated(cfg, i) for i in range(len(cfg.units)))
-    assert n == 1 + s.info.n_classes * (2 + 3 * cfg.muon.ns_steps) + int(rest)
+    classes = {(min(u.rows, u.cols), max(u.rows, u.cols)) for u in cfg.units}
+    per_class = [2 + (1 if -(-m // 128) == 1 else 3 * cfg.muon.ns_steps) for m, _ in classes]
+    assert len(classes) == s.info.n_classes
+    assert n == 1 + sum(per_class) + int(rest)
 
 
 def test_newton_schulz_ragged_row_tails(hm, dev):
