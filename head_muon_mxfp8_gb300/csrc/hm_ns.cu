@@ -475,13 +475,60 @@ __device__ __forceinline__ bool chunk_w_blocks(const GemmParams& p, const NsUnit
     return true;
 }
 
-// f2 and G of the chunk's w blocks from their loaded values (w0, w1: this
-// lane's 8 elements of block s) and the staged v.
-__device__ __forceinline__ void update_w_blocks(const GemmParams& p, const NsUnit& nu, const float* stage,
-                                                const int64_t (&dst)[4], const float4 (&w0)[4], const float4 (&w1)[4]) {
+// v of this lane's part of block s of the chunk, from the warp's staging tile
+__device__ __forceinline__ void staged_block(const float* stage, bool tr, int s, float (&y)[8]) {
+    const int lane = threadIdx.x & 31;
+    const int cq = (lane & 3) * 8;
+    const int kk = (lane >> 2) + 8 * s;
+    if (tr) {
+        stage_col8(stage, cq, kk, y);  // column kk of the chunk, rows cq..cq+7
+    } else {
+        const float4 a = stage4_ld(stage, kk, cq >> 2);
+        const float4 b = stage4_ld(stage, kk, (cq >> 2) + 1);
+        y[0] = a.x; y[1] = a.y; y[2] = a.z; y[3] = a.w;
+        y[4] = b.x; y[5] = b.y; y[6] = b.z; y[7] = b.w;
+    }
+}
+
+// Last product with the update folded in (units flagged kNsEpiUpdate): the
+// chunk's 32 x 32 values of v = aX + BX (fp32, in the warp's swizzled staging
+// tile) never reach memory.  Each 1 x 32 MX block of the unit's w that the
+// chunk covers -- a row of the chunk, or a column when the unit is stored
+// transposed (X = u^T) -- is read from the root, updated as f2 does it
+// (w*decay - step*v, or w - step*v, each product and the difference rounded
+// once) and quantized as G does it, so w, q and s come out bit-identical to
+// the pass through v.  Four lanes own one block, 8 elements each (lane l:
+// block l/4 + 8s, elements 8(l%4)..+7); the loads of all four blocks go first.
+// (Issuing them before the aX addend is folded in, or a tile ahead as L2
+// prefetches, measured no faster.)
+//
+// base1: root offset minus unit offset of a unit with one fragment (a local
+// unit), read once per tile; -1 = look the fragment up per block.
+__device__ __forceinline__ void final_update_chunk(const GemmParams& p, const NsUnit& nu, int64_t base1,
+                                                   const float* stage, int i0, int j0) {
     const int lane = threadIdx.x & 31;
     const bool tr = nu.flags & kNsTransposed;
+    const int kw = tr ? p.m_real : p.n_real;      // length of a row of w (the MX K)
+    const int rows_w = tr ? p.n_real : p.m_real;  // rows of w
+    const int rw0 = tr ? j0 : i0;                  // w row of the chunk's block 0
+    const int cw0 = tr ? i0 : j0;                  // w column of every block's first element
+    if (cw0 >= kw) return;                         // padding of X (warp-uniform)
     const int cq = (lane & 3) * 8;
+    int64_t dst[4];
+    float4 w0[4], w1[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int rw = rw0 + (lane >> 2) + 8 * s;
+        w0[s] = w1[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dst[s] = -1;
+        if (rw >= rows_w) continue;
+        // the unit's fragment that holds this block (32-aligned: the whole block)
+        const int64_t e = static_cast<int64_t>(rw) * kw + cw0;
+        dst[s] = base1 >= 0 ? base1 + e : unit_root_offset(p, nu, e);
+        const float4* wp = reinterpret_cast<const float4*>(p.w + dst[s] + cq);
+        w0[s] = __ldcs(wp);
+        w1[s] = __ldcs(wp + 1);
+    }
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const int kk = (lane >> 2) + 8 * s;
@@ -519,37 +566,6 @@ __device__ __forceinline__ void update_w_blocks(const GemmParams& p, const NsUni
         __stcs(reinterpret_cast<uint2*>(p.q + dst[s] + cq), make_uint2(c01 | (c23 << 16), c45 | (c67 << 16)));
         if ((lane & 3) == 0) p.s[dst[s] >> 5] = static_cast<uint8_t>(ex + 127);
     }
-}
-
-// Last product with the update folded in (units flagged kNsEpiUpdate): the
-// chunk's 32 x 32 values of v = aX + BX (fp32, in the warp's swizzled staging
-// tile) never reach memory.  Each 1 x 32 MX block of the unit's w that the
-// chunk covers -- a row of the chunk, or a column when the unit is stored
-// transposed (X = u^T) -- is read from the root, updated as f2 does it
-// (w*decay - step*v, or w - step*v, each product and the difference rounded
-// once) and quantized as G does it, so w, q and s come out bit-identical to
-// the pass through v.  Four lanes own one block, 8 elements each (lane l:
-// block l/4 + 8s, elements 8(l%4)..+7); the loads of all four blocks go first.
-// (Issuing them before the aX addend is folded in, or a tile ahead as L2
-// prefetches, measured no faster.)
-//
-// base1: root offset minus unit offset of a unit with one fragment (a local
-// unit), read once per tile; -1 = look the fragment up per block.
-__device__ __forceinline__ void final_update_chunk(const GemmParams& p, const NsUnit& nu, int64_t base1,
-                                                   const float* stage, int i0, int j0) {
-    int64_t dst[4];
-    if (!chunk_w_blocks(p, nu, base1, i0, j0, dst)) return;
-    const int cq = (threadIdx.x & 3) * 8;
-    float4 w0[4], w1[4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        w0[s] = w1[s] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (dst[s] < 0) continue;
-        const float4* wp = reinterpret_cast<const float4*>(p.w + dst[s] + cq);
-        w0[s] = __ldcs(wp);
-        w1[s] = __ldcs(wp + 1);
-    }
-    update_w_blocks(p, nu, stage, dst, w0, w1);
 }
 
 // The last product's 32 x 32 chunk (rows i0.., columns j0.. of X; this lane's
@@ -1195,6 +1211,7 @@ constexpr int kSmallThreads = 352;
 constexpr int kSmallRing = 5;                // X tiles in flight
 constexpr int kSmallNB = 4;                  // B X accumulators
 constexpr int kSmallTile = 128 * 64 * 2;     // a 128 x 64 bf16 tile (16 KB)
+constexpr int kSmallWGroup = 1;              // w blocks updated together in the last pass (1, 2, 4 measured alike)
 struct SmallCfg {
     static constexpr int RING_OFF = 0;
     static constexpr int AS_OFF = RING_OFF + kSmallRing * kSmallTile;  // A, bf16: two [128][64] K atoms
@@ -1253,20 +1270,66 @@ __device__ __forceinline__ void prefetch_w_chunk(const GemmParams& p, const NsUn
         cp_async16(buf + ((2 * s + 1) * 32 + lane) * 16, src + 4);
     }
 }
+// G blocks at a time, interleaved: the element updates, the amax trees (max is
+// exact, so the order does not matter), the shuffles and the stores of the G
+// blocks are independent chains the warp can overlap.
+template <int G>
+__device__ __forceinline__ void update_w_group(const GemmParams& p, float step, float (&x)[G][8], const float (&wv)[G][8],
+                                               const int64_t* dst, int cq) {
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float a = p.has_decay ? __fmul_rn(wv[g][e], p.decay) : wv[g][e];
+            x[g][e] = __fsub_rn(a, __fmul_rn(step, x[g][e]));
+        }
+    float am[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float m01 = fmaxf(fabsf(x[g][0]), fabsf(x[g][1])), m23 = fmaxf(fabsf(x[g][2]), fabsf(x[g][3]));
+        const float m45 = fmaxf(fabsf(x[g][4]), fabsf(x[g][5])), m67 = fmaxf(fabsf(x[g][6]), fabsf(x[g][7]));
+        am[g] = fmaxf(fmaxf(m01, m23), fmaxf(m45, m67));
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) am[g] = fmaxf(am[g], __shfl_xor_sync(0xffffffffu, am[g], 1));
+#pragma unroll
+    for (int g = 0; g < G; ++g) am[g] = fmaxf(am[g], __shfl_xor_sync(0xffffffffu, am[g], 2));
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        if (dst[g] < 0) continue;  // a row of w beyond the unit (same for the block's 4 lanes)
+        float4* wp = reinterpret_cast<float4*>(p.w + dst[g] + cq);
+        __stcs(wp, make_float4(x[g][0], x[g][1], x[g][2], x[g][3]));
+        __stcs(wp + 1, make_float4(x[g][4], x[g][5], x[g][6], x[g][7]));
+        const int ex = mx_scale_exponent(am[g]);
+        const float sc = mx_inv_scale(ex);
+        const uint32_t c01 = cvt_e4m3x2(x[g][0] * sc, x[g][1] * sc);
+        const uint32_t c23 = cvt_e4m3x2(x[g][2] * sc, x[g][3] * sc);
+        const uint32_t c45 = cvt_e4m3x2(x[g][4] * sc, x[g][5] * sc);
+        const uint32_t c67 = cvt_e4m3x2(x[g][6] * sc, x[g][7] * sc);
+        __stcs(reinterpret_cast<uint2*>(p.q + dst[g] + cq), make_uint2(c01 | (c23 << 16), c45 | (c67 << 16)));
+        if ((threadIdx.x & 3) == 0) p.s[dst[g] >> 5] = static_cast<uint8_t>(ex + 127);
+    }
+}
+
+template <int G>
 __device__ __forceinline__ void final_update_chunk_buf(const GemmParams& p, const NsUnit& nu, int64_t base1,
                                                        const float* stage, int i0, int j0, const float4* buf) {
     int64_t dst[4];
     if (!chunk_w_blocks(p, nu, base1, i0, j0, dst)) return;
     const int lane = threadIdx.x & 31;
-    float4 w0[4], w1[4];
+    const bool tr = nu.flags & kNsTransposed;
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        w0[s] = w1[s] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (dst[s] < 0) continue;
-        w0[s] = buf[(2 * s) * 32 + lane];
-        w1[s] = buf[(2 * s + 1) * 32 + lane];
+    for (int s0 = 0; s0 < 4; s0 += G) {
+        float x[G][8], wv[G][8];  // x holds the staged v, then the new w
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            staged_block(stage, tr, s0 + g, x[g]);
+            const float4 a = buf[(2 * (s0 + g)) * 32 + lane], b = buf[(2 * (s0 + g) + 1) * 32 + lane];
+            wv[g][0] = a.x; wv[g][1] = a.y; wv[g][2] = a.z; wv[g][3] = a.w;
+            wv[g][4] = b.x; wv[g][5] = b.y; wv[g][6] = b.z; wv[g][7] = b.w;
+        }
+        update_w_group<G>(p, nu.step, x, wv, dst + s0, (lane & 3) * 8);
     }
-    update_w_blocks(p, nu, stage, dst, w0, w1);
 }
 
 __global__ void __launch_bounds__(kSmallThreads, 1)
@@ -1570,7 +1633,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                 // w buffers of the last pass: the 4 KB of A that this warp wrote (idle
                 // once B is formed) and a 4 KB block of the X' tiles, which the last
                 // pass does not store
-                uint8_t* wbuf[2] = {as + h * kSmallTile + q * 4096, xo + h * kSmallTile + q * 4096};
+                const uint32_t wbuf0 = smem_u32(as + h * kSmallTile + q * 4096);
+                const uint32_t wstep = static_cast<uint32_t>(xo - as);  // buffer 1 - buffer 0
                 if (last) {
                     nu = p.ns_units[u];
                     fuse = p.fuse_update && (nu.flags & kNsEpiUpdate);
@@ -1582,7 +1646,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                     if (ok && xg >= 2) ok = mbar_wait(smem_u32(&xs_done[(xg - 2) & 1]), ((xg - 2) >> 1) & 1, p.err, bail);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
-                    prefetch_w_chunk(p, nu, base1, q * 32, tile_of(S, 0) * 64 + h * 32, smem_u32(wbuf[0]));
+                    prefetch_w_chunk(p, nu, base1, q * 32, tile_of(S, 0) * 64 + h * 32, wbuf0);
                     cp_async_commit();
                 }
                 // the pass over X: X' = a X + B X per tile
@@ -1592,7 +1656,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                     if (fuse) {
                         if (t + 1 < nt)
                             prefetch_w_chunk(p, nu, base1, q * 32, tile_of(S, t + 1) * 64 + h * 32,
-                                             smem_u32(wbuf[(t + 1) & 1]));
+                                             wbuf0 + ((t + 1) & 1) * wstep);
                         cp_async_commit();
                     }
                     ok = mbar_wait(smem_u32(&d_full[db]), (dpos / kSmallNB) & 1, p.err, bail);
@@ -1657,8 +1721,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                         __syncwarp();
                         if (fuse) {
                             cp_async_wait_1();  // this tile's w (the next tile's may be in flight)
-                            final_update_chunk_buf(p, nu, base1, stage, q * 32, j * 64 + h * 32,
-                                                   reinterpret_cast<const float4*>(wbuf[t & 1]));
+                            final_update_chunk_buf<kSmallWGroup>(p, nu, base1, stage, q * 32, j * 64 + h * 32,
+                                                   reinterpret_cast<const float4*>(as + h * kSmallTile + q * 4096 +
+                                                                                   (t & 1) * wstep));
                         } else {
                             store_final_chunk(p, nu, fuse, base1, stage, row, q * 32, j * 64 + h * 32);
                         }
