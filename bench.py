@@ -81,11 +81,13 @@ def straddling_elems(cfg, plan_info) -> int:
 
 
 # DRAM bytes (read + write) of one Newton-Schulz stage of the Video-DiT x8
-# workload with f2 and G folded into its last products (prepare, norm and 30
-# GEMM launches of the timed update), summed from an ncu launch list of
-# dram__bytes_read.sum + dram__bytes_write.sum; valid only for the kernel
-# source it was measured on (sha256 prefix of hm_ns.cu).
-NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.751e+11, "hm_ns_sha256": "ed1104c8bcff3862"}
+# workload with f2 and G folded into its last products: an ncu launch list of
+# dram__bytes_read.sum + dram__bytes_write.sum over the timed update of one
+# Video-DiT layer (prepare, norm, the one-launch head-class kernel and 15
+# CTA-pair GEMMs: 19.89 GB), scaled by the units processed (x8); valid only
+# for the kernel source it was measured on (sha256 prefix of hm_ns.cu).
+NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.591e+11, "hm_ns_sha256": "a9bfd7c4d85394d0",
+                    "how": "one Video-DiT layer measured, x8 by units"}
 
 
 def ns_stage_traffic(cfg):
@@ -473,10 +475,10 @@ def run_ours(args, cfg):
             v["frac_of_8tbs"] = v["gbs"] / 8000.0
     roofline = {"bound": "tensor", "achieved": ns_tflops, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                 "frac": ns_tflops / peaks["bf16_sustained"], "traffic": ns_stage_traffic(cfg),
-                "traffic_unit": "DRAM bytes per Newton-Schulz stage (one update), ncu",
-                "kernel": "Newton-Schulz stage: ns_gemm_kernel / ns_gemm_pair_kernel (3 products x 5 iterations "
-                          "per shape class) + norm/prepare; the last product also applies f2 and the MXFP8 "
-                          "requant (timed with them)",
+                "traffic_unit": "DRAM bytes per Newton-Schulz stage (one update), ncu: " + NS_STAGE_TRAFFIC["how"],
+                "kernel": "Newton-Schulz stage: per shape class prepare + norm, then ns_small_kernel (Gram size "
+                          "128: every iteration in one launch) or ns_gemm_kernel / ns_gemm_pair_kernel (3 products "
+                          "x 5 iterations); the last product also applies f2 and the MXFP8 requant (timed with them)",
                 "peak_kind": f"bf16 dense sustained ({peaks['source']})",
                 "frac_of_burst": ns_tflops / peaks["bf16"],
                 "note": "achieved counts the algorithmic 5(4m^2n+2m^3) FLOP per unit; the kernels skip the "
