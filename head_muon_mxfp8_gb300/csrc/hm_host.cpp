@@ -370,6 +370,9 @@ struct hm_muon_plan {
     char* ws = nullptr;
     std::vector<ClassMaps> maps;
     mutable float f2_lr = NAN;
+    // f0 ran with u as scratch: X0 and the unit scales of every class are in the
+    // workspace, so the next Newton-Schulz stage skips the prepare pass
+    mutable bool x0_ready = false;
     mutable int f2_alpha_mode = -1;
 };
 
@@ -473,12 +476,12 @@ extern "C" hm_status muon_plan(hm_muon_plan** out, const hm_chain* chain, const 
             nu.v_off = nu.u_off;
             nu.flags = (q.local ? 0 : (hm::kNsUStaged | hm::kNsVStaged)) |
                        (u.rows > u.cols ? hm::kNsTransposed : 0);
-            if (q.epi) {
-                nu.flags |= hm::kNsEpiUpdate;
-                nu.frag0 = static_cast<int32_t>(p->ns_frags.size());
-                nu.nfrag = static_cast<int32_t>(q.frags.size());
-                for (const hm_fragment& f : q.frags) p->ns_frags.push_back(NsFrag{f.unit_offset, f.root_offset});
-            }
+            if (q.epi) nu.flags |= hm::kNsEpiUpdate;
+            // every unit's fragments: f0 folded into the prepare pass reads g and m
+            // through them; the last product's f2 + G writes w, q and s through them
+            nu.frag0 = static_cast<int32_t>(p->ns_frags.size());
+            nu.nfrag = static_cast<int32_t>(q.frags.size());
+            for (const hm_fragment& f : q.frags) p->ns_frags.push_back(NsFrag{f.unit_offset, f.root_offset});
             p->ns_units.push_back(nu);
         }
         p->classes.push_back(c);
@@ -705,6 +708,7 @@ extern "C" hm_status muon_plan_upload(hm_muon_plan* p, void* workspace, size_t w
     }
     p->ws = ws;
     p->f2_lr = NAN;  // force the f2 steps to be written on the next update
+    p->x0_ready = false;
     p->f2_alpha_mode = -1;
     return HM_OK;
 }
@@ -799,14 +803,28 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
     float* v_stage = reinterpret_cast<float*>(ws + p->off_vstage);
 
     if ((stages & HM_STAGE_F2) && (st = refresh_steps(p, hp, s)) != HM_OK) return st;
-    if (fused && (stages & HM_STAGE_F0)) {
+    if (fused && (stages & HM_STAGE_F0) && skip_v) {
+        // u as scratch: f0 runs inside the prepare pass of every shape class,
+        // reading g and m through the units' fragments and writing X0 and the
+        // norm's partial sums instead of u; the unit scales follow, and the next
+        // Newton-Schulz stage on this plan starts from them
+        const NsFrag* frags = reinterpret_cast<const NsFrag*>(ws + p->off_nsf);
+        for (size_t k = 0; k < p->classes.size(); ++k) {
+            const NsClassDev& c = p->classes[k];
+            const NsUnit* units_dev = reinterpret_cast<const NsUnit*>(ws + p->off_nsu) + c.first_unit;
+            if (hm::launch_ns_f0_prepare(c, units_dev, frags, b->m, b->g, hp->momentum, hp->nesterov, ws, s) !=
+                    cudaSuccess ||
+                hm::launch_ns_norm(c, ws, hp->eps, s) != cudaSuccess)
+                return HM_ERR_CUDA;
+        }
+        p->x0_ready = true;
+    } else if (fused && (stages & HM_STAGE_F0)) {
         // f0 writes u of straddling fragments into their staging as well
         RangeArgs ra = device_ranges(ws, p->off_f0x, p->f0x_tab);
-        // with v skipped, u of straddling units goes to their staging only: the
-        // Newton-Schulz stage reads it there and nothing reads the root copy
-        if (hm::launch_f0(ra, b->m, b->g, b->u, u_stage, hp->momentum, hp->nesterov, skip_v, s) != cudaSuccess)
+        if (hm::launch_f0(ra, b->m, b->g, b->u, u_stage, hp->momentum, hp->nesterov, 0, s) != cudaSuccess)
             return HM_ERR_CUDA;
     }
+    if ((stages & HM_STAGE_F0) && !(fused && skip_v)) p->x0_ready = false;  // u written: prepare from it
     if (!fused && (stages & HM_STAGE_F0)) {
         RangeArgs ra = device_ranges(ws, p->off_seg, p->seg_tab);
         if (hm::launch_f0(ra, b->m, b->g, b->u, nullptr, hp->momentum, hp->nesterov, 0, s) != cudaSuccess)
@@ -823,13 +841,15 @@ extern "C" hm_status muon_update_units(const hm_muon_plan* p, const hm_muon_bufs
         // HM_ERR_TIMEOUT in the device error word.
         const char* inj = std::getenv("HM_INJECT_NS_WAIT_TIMEOUT");
         bool inject = inj && inj[0] == '1';
+        const bool have_x0 = p->x0_ready;  // X0 and the unit scales left by f0 with u as scratch
+        p->x0_ready = false;
 
         for (size_t k = 0; k < p->classes.size(); ++k) {
             const NsClassDev& c = p->classes[k];
             const ClassMaps& mp = p->maps[k];
             const NsUnit* units_dev = reinterpret_cast<const NsUnit*>(ws + p->off_nsu) + c.first_unit;
-            if (hm::launch_ns_prepare(c, units_dev, b->u, u_stage, ws, s) != cudaSuccess ||
-                hm::launch_ns_norm(c, ws, hp->eps, s) != cudaSuccess)
+            if (!have_x0 && (hm::launch_ns_prepare(c, units_dev, b->u, u_stage, ws, s) != cudaSuccess ||
+                             hm::launch_ns_norm(c, ws, hp->eps, s) != cudaSuccess))
                 return HM_ERR_CUDA;
             const float* inv = reinterpret_cast<const float*>(ws + c.inv_off);
             if (c.mp == 128) {

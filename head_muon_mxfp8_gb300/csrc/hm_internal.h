@@ -49,7 +49,7 @@ struct NsUnit {
     int32_t cols;
     int32_t flags;   // kNs* bits
     float   step;    // kNsEpiUpdate: fp32(lr * alpha), as in the f2 table
-    int32_t frag0;   // kNsEpiUpdate: first of the unit's nfrag entries in the fragment table
+    int32_t frag0;   // first of the unit's nfrag entries in the fragment table (unit order)
     int32_t nfrag;
 };
 static_assert(sizeof(NsUnit) == 40, "NsUnit layout");
@@ -225,6 +225,11 @@ cudaError_t launch_reduce_scatter(const RangeArgs& ra, const RsArgs& a, float* g
 cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, const uint16_t* u_root,
                               const uint16_t* u_stage, char* ws, cudaStream_t st);
 cudaError_t launch_ns_norm(const NsClassDev& c, char* ws, float eps, cudaStream_t st);
+// f0 of every element of the class's units (m updated where it lives in the
+// rank segments) with u going straight into X0 and the norm's partial sums:
+// the prepare pass without a stored u (frags: every unit's fragment table)
+cudaError_t launch_ns_f0_prepare(const NsClassDev& c, const NsUnit* units_dev, const NsFrag* frags_dev, float* m,
+                                 const float* g, float mu, int nesterov, char* ws, cudaStream_t st);
 // b_mn: the B operand is MN-major (its map has 64 x 64 boxes, N innermost)
 cudaError_t launch_ns_gemm(const CUtensorMap& tma, const CUtensorMap& tmb, const GemmParams& p,
                            int bn, int b_mn, cudaStream_t st);

@@ -163,6 +163,144 @@ __global__ void __launch_bounds__(kPrepThreads) ns_prepare_kernel(const NsUnit* 
     }
 }
 
+__device__ __forceinline__ uint32_t bf16_rne_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+
+// ---------------------------------------------------------------------------
+// f0 folded into the prepare pass (u as scratch): each 8-element chunk of u is
+// computed from the main gradient and the momentum where they live in the
+// rank segments (m <- mu*m + g, multiply then add, each rounded; u =
+// bf16_RNE(m), or bf16_RNE(g + mu*m) with Nesterov -- f0's arithmetic), m is
+// written back, and u goes straight into X0 with the same tile mapping,
+// transposition and per-tile sums of squares as ns_prepare_kernel, so the
+// norm and X0 are bit-identical to preparing from a stored u.  u itself is
+// never written.  A chunk's elements lie in one fragment when u's row length
+// is a multiple of 8 (fragments start on multiples of 32 unit elements);
+// otherwise every element looks its fragment up.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPrepThreads) f0_prepare_kernel(const NsUnit* __restrict__ units,
+                                                                   const NsFrag* __restrict__ frags,
+                                                                   float* __restrict__ m_root,
+                                                                   const float* __restrict__ g_root, float mu,
+                                                                   int nesterov, float* __restrict__ partials,
+                                                                   uint16_t* __restrict__ X, int m, int n, int np) {
+    __shared__ __align__(16) uint16_t T[64][64];
+    __shared__ float red[kPrepThreads / 32];
+    auto tx = [](int r, int c) { return ((((c >> 3) ^ (r >> 3)) & 7) << 3) | (c & 7); };
+    const int unit = blockIdx.z;
+    const NsUnit nu = units[unit];
+    const bool tr = nu.flags & kNsTransposed;
+    const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+    const int ld = tr ? m : n;
+    const bool vec_ok = (ld & 7) == 0;
+    const int rlim = tr ? n : m, clim = tr ? m : n;
+    const NsFrag* fr = frags + nu.frag0;
+    const int nf = nu.nfrag;
+    const int64_t base1 = nf == 1 ? fr[0].root_off - fr[0].unit_off : -1;
+    auto root_of = [&](int64_t e) -> int64_t {
+        if (base1 >= 0) return base1 + e;
+        int f = 0;
+        while (f + 1 < nf && fr[f + 1].unit_off <= e) ++f;
+        return fr[f].root_off + (e - fr[f].unit_off);
+    };
+    auto f0_of = [&](float g, float& mv) {  // returns u (as float) and updates m
+        mv = __fadd_rn(__fmul_rn(mu, mv), g);
+        return nesterov ? __fadd_rn(g, __fmul_rn(mu, mv)) : mv;
+    };
+    // loads of all four chunks first
+    float4 gv[4][2], mv[4][2];
+    int64_t ro[4];
+    bool full[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int v = threadIdx.x + t * kPrepThreads;
+        const int a = v >> 3, b0 = (v & 7) * 8;
+        const int ur = (tr ? j0 : i0) + a, uc = (tr ? i0 : j0) + b0;
+        full[t] = ur < rlim && vec_ok && uc + 8 <= clim;
+        ro[t] = 0;
+        if (full[t]) {
+            ro[t] = root_of(static_cast<int64_t>(ur) * ld + uc);
+            const float4* gp = reinterpret_cast<const float4*>(g_root + ro[t]);
+            const float4* mp = reinterpret_cast<const float4*>(m_root + ro[t]);
+            gv[t][0] = __ldcs(gp);
+            gv[t][1] = __ldcs(gp + 1);
+            mv[t][0] = __ldcs(mp);
+            mv[t][1] = __ldcs(mp + 1);
+        }
+    }
+    uint4 raw[4];  // 8 bf16 of u per chunk, zero outside the unit
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int v = threadIdx.x + t * kPrepThreads;
+        const int a = v >> 3, b0 = (v & 7) * 8;
+        const int ur = (tr ? j0 : i0) + a, uc = (tr ? i0 : j0) + b0;
+        if (full[t]) {
+            const float g8[8] = {gv[t][0].x, gv[t][0].y, gv[t][0].z, gv[t][0].w,
+                                 gv[t][1].x, gv[t][1].y, gv[t][1].z, gv[t][1].w};
+            float m8[8] = {mv[t][0].x, mv[t][0].y, mv[t][0].z, mv[t][0].w, mv[t][1].x, mv[t][1].y, mv[t][1].z, mv[t][1].w};
+            float u8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) u8[k] = f0_of(g8[k], m8[k]);
+            float4* mp = reinterpret_cast<float4*>(m_root + ro[t]);
+            __stcs(mp, make_float4(m8[0], m8[1], m8[2], m8[3]));
+            __stcs(mp + 1, make_float4(m8[4], m8[5], m8[6], m8[7]));
+            raw[t] = make_uint4(bf16_rne_bits(u8[0]) | (bf16_rne_bits(u8[1]) << 16), bf16_rne_bits(u8[2]) | (bf16_rne_bits(u8[3]) << 16),
+                                bf16_rne_bits(u8[4]) | (bf16_rne_bits(u8[5]) << 16), bf16_rne_bits(u8[6]) | (bf16_rne_bits(u8[7]) << 16));
+        } else {
+            uint32_t h[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                h[k] = 0u;
+                if (ur < rlim && uc + k < clim) {
+                    const int64_t r = root_of(static_cast<int64_t>(ur) * ld + uc + k);
+                    float mk = m_root[r];
+                    const float uk = f0_of(g_root[r], mk);
+                    m_root[r] = mk;
+                    h[k] = bf16_rne_bits(uk);
+                }
+            }
+            raw[t] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+        }
+    }
+    float sq = 0.f;  // this thread's 32 values, in a fixed order (that of ns_prepare_kernel)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int v = threadIdx.x + t * kPrepThreads;
+        const int a = v >> 3, b0 = (v & 7) * 8;
+        const uint32_t w[4] = {raw[t].x, raw[t].y, raw[t].z, raw[t].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+            sq = fmaf(lo, lo, sq);
+            sq = fmaf(hi, hi, sq);
+        }
+        if (!tr) {
+            *reinterpret_cast<uint4*>(&T[a][tx(a, b0)]) = raw[t];
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                T[b0 + k][tx(b0 + k, a)] = static_cast<uint16_t>(k & 1 ? w[k >> 1] >> 16 : w[k >> 1] & 0xFFFFu);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sq;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int k = 0; k < kPrepThreads / 32; ++k) tot += red[k];
+        partials[static_cast<int64_t>(unit) * gridDim.x * gridDim.y + blockIdx.y * gridDim.x + blockIdx.x] = tot;
+    }
+    uint16_t* xo = X + static_cast<int64_t>(unit) * gridDim.y * 64 * np;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int v = threadIdx.x + t * kPrepThreads;
+        const int ii = v >> 3, jj = (v & 7) * 8;
+        *reinterpret_cast<uint4*>(xo + static_cast<int64_t>(i0 + ii) * np + j0 + jj) =
+            *reinterpret_cast<const uint4*>(&T[ii][tx(ii, jj)]);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // PTX wrappers: mbarrier, TMA, tcgen05
 // ---------------------------------------------------------------------------
@@ -1208,7 +1346,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // Every wait is bounded, as in the GEMM kernels.
 // ---------------------------------------------------------------------------
 constexpr int kSmallThreads = 352;
-constexpr int kSmallRing = 5;                // X tiles in flight
+constexpr int kSmallRing = 4;                // X tiles in flight
+constexpr int kSmallXo = 4;                  // X' tiles in shared memory (written, awaiting the A MMA and the store)
+constexpr int kSmallLag = 2;                 // the A MMA of X'_j is issued after the B X of tile j + kSmallLag
+static_assert(kSmallXo >= kSmallLag + 1 && kSmallXo >= 2, "X' buffers");
 constexpr int kSmallNB = 4;                  // B X accumulators
 constexpr int kSmallTile = 128 * 64 * 2;     // a 128 x 64 bf16 tile (16 KB)
 constexpr int kSmallWGroup = 1;              // w blocks updated together in the last pass (1, 2, 4 measured alike)
@@ -1216,8 +1357,8 @@ struct SmallCfg {
     static constexpr int RING_OFF = 0;
     static constexpr int AS_OFF = RING_OFF + kSmallRing * kSmallTile;  // A, bf16: two [128][64] K atoms
     static constexpr int BS_OFF = AS_OFF + 2 * kSmallTile;              // B, bf16: the same layout
-    static constexpr int XO_OFF = BS_OFF + 2 * kSmallTile;              // X' tiles, two buffers
-    static constexpr int ST_OFF = XO_OFF + 2 * kSmallTile;              // per epilogue warp a 32 x 32 fp32 tile
+    static constexpr int XO_OFF = BS_OFF + 2 * kSmallTile;              // X' tiles
+    static constexpr int ST_OFF = XO_OFF + kSmallXo * kSmallTile;       // per epilogue warp a 32 x 32 fp32 tile
     static constexpr int BAR_OFF = ST_OFF + kEpiWarps * 32 * 32 * 4;
     static constexpr int SMEM = BAR_OFF + 512 + 1024;
     // kind::f16, D fp32, A and B bf16: M = N = 128 with both operands K-major
@@ -1351,9 +1492,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     uint64_t* d_full = x_eepi + kSmallRing;
     uint64_t* d_empty = d_full + kSmallNB;
     uint64_t* xo_full = d_empty + kSmallNB;    // X' tile written (for the Gram MMA and the store)
-    uint64_t* xo_free = xo_full + 2;           // its Gram MMA done
-    uint64_t* xs_done = xo_free + 2;           // its TMA store has read it
-    uint64_t* gram_full = xs_done + 2;         // A complete in TMEM
+    uint64_t* xo_free = xo_full + kSmallXo;    // its Gram MMA done
+    uint64_t* xs_done = xo_free + kSmallXo;    // its TMA store has read it
+    uint64_t* gram_full = xs_done + kSmallXo;  // A complete in TMEM
     uint64_t* a_ready = gram_full + 1;         // A in shared memory
     uint64_t* aa_full = a_ready + 1;           // AA complete in TMEM
     uint64_t* b_ready = aa_full + 1;           // B in shared memory
@@ -1374,7 +1515,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
             mbar_init(smem_u32(&d_full[b]), 1);
             mbar_init(smem_u32(&d_empty[b]), kEpiWarps);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kSmallXo; ++b) {
             mbar_init(smem_u32(&xo_full[b]), kEpiWarps);
             mbar_init(smem_u32(&xo_free[b]), 1);
             mbar_init(smem_u32(&xs_done[b]), 1);
@@ -1500,25 +1641,28 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                         umma_commit(smem_u32(&d_full[db]));
                         ++dpos;
                         ++pos;
-                        if (!last && t >= 1) {
-                            // the next A from the previous tile's X' (one tile behind, so the
-                            // B X of this tile is issued before waiting for that epilogue)
-                            const int b = xg & 1;
-                            if (!mbar_wait(smem_u32(&xo_full[b]), (xg >> 1) & 1, p.err, bail)) { ok = false; break; }
+                        if (!last && t >= kSmallLag) {
+                            // the next A from the X' of tile t - kSmallLag: the MMA runs kSmallLag
+                            // tiles of B X ahead of the epilogue instead of waiting for it
+                            const int b = xg % kSmallXo;
+                            if (!mbar_wait(smem_u32(&xo_full[b]), (xg / kSmallXo) & 1, p.err, bail)) { ok = false; break; }
                             tc_fence_after();
-                            gram_on(smem_u32(xo + b * kSmallTile), t > 1);
+                            gram_on(smem_u32(xo + b * kSmallTile), t > kSmallLag);
                             umma_commit(smem_u32(&xo_free[b]));
                             ++xg;
                         }
                     }
                     if (!ok) break;
                     if (!last) {
-                        const int b = xg & 1;
-                        if (!mbar_wait(smem_u32(&xo_full[b]), (xg >> 1) & 1, p.err, bail)) { ok = false; break; }
-                        tc_fence_after();
-                        gram_on(smem_u32(xo + b * kSmallTile), nt > 1);
-                        umma_commit(smem_u32(&xo_free[b]));
-                        ++xg;
+                        for (int g = nt > kSmallLag ? nt - kSmallLag : 0; g < nt && ok; ++g) {
+                            const int b = xg % kSmallXo;
+                            if (!mbar_wait(smem_u32(&xo_full[b]), (xg / kSmallXo) & 1, p.err, bail)) { ok = false; break; }
+                            tc_fence_after();
+                            gram_on(smem_u32(xo + b * kSmallTile), g > 0);
+                            umma_commit(smem_u32(&xo_free[b]));
+                            ++xg;
+                        }
+                        if (!ok) break;
                         umma_commit(smem_u32(gram_full));
                     }
                 }
@@ -1535,8 +1679,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                 for (int it = 0; it + 1 < S && ok; ++it) {
                     const CUtensorMap* map = ((it + 1) & 1) ? &tx1 : &tx0;
                     for (int t = 0; t < nt; ++t) {
-                        const int b = xg & 1;
-                        if (!mbar_wait(smem_u32(&xo_full[b]), (xg >> 1) & 1, p.err, bail)) { ok = false; break; }
+                        const int b = xg % kSmallXo;
+                        if (!mbar_wait(smem_u32(&xo_full[b]), (xg / kSmallXo) & 1, p.err, bail)) { ok = false; break; }
                         tma_store_3d(map, smem_u32(xo + b * kSmallTile), tile_of(it + 1, t) * 64, 0, u);
                         bulk_commit();
                         bulk_wait_read_all();
@@ -1642,8 +1786,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                 }
                 if (fuse) {
                     // the X' tiles' last stores have read them
-                    if (xg >= 1) ok = mbar_wait(smem_u32(&xs_done[(xg - 1) & 1]), ((xg - 1) >> 1) & 1, p.err, bail);
-                    if (ok && xg >= 2) ok = mbar_wait(smem_u32(&xs_done[(xg - 2) & 1]), ((xg - 2) >> 1) & 1, p.err, bail);
+                    for (int k = 1; k <= kSmallXo && k <= xg && ok; ++k)
+                        ok = mbar_wait(smem_u32(&xs_done[(xg - k) % kSmallXo]), ((xg - k) / kSmallXo) & 1, p.err, bail);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     prefetch_w_chunk(p, nu, base1, q * 32, tile_of(S, 0) * 64 + h * 32, wbuf0);
@@ -1694,10 +1838,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                     }
                     if (!last) {
                         // bf16 X' into its shared tile, for the next A and the store
-                        const int b = xg & 1;
-                        if (xg >= 2) {
-                            ok = mbar_wait(smem_u32(&xo_free[b]), ((xg >> 1) - 1) & 1, p.err, bail) &&
-                                 mbar_wait(smem_u32(&xs_done[b]), ((xg >> 1) - 1) & 1, p.err, bail);
+                        const int b = xg % kSmallXo;
+                        if (xg >= kSmallXo) {
+                            ok = mbar_wait(smem_u32(&xo_free[b]), ((xg / kSmallXo) - 1) & 1, p.err, bail) &&
+                                 mbar_wait(smem_u32(&xs_done[b]), ((xg / kSmallXo) - 1) & 1, p.err, bail);
                             ok = __all_sync(0xffffffffu, ok);
                             if (!ok) break;
                         }
@@ -1824,6 +1968,16 @@ cudaError_t launch_ns_prepare(const NsClassDev& c, const NsUnit* units_dev, cons
     note_launch();
     ns_prepare_kernel<<<g, kPrepThreads, 0, st>>>(units_dev, u_root, u_stage, reinterpret_cast<float*>(ws + c.part_off),
                                                   reinterpret_cast<uint16_t*>(ws + c.x_off[0]), c.m, c.n, c.np);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ns_f0_prepare(const NsClassDev& c, const NsUnit* units_dev, const NsFrag* frags_dev, float* m,
+                                 const float* g, float mu, int nesterov, char* ws, cudaStream_t st) {
+    dim3 grid(c.np / 64, c.mp / 64, c.n_units);
+    note_launch();
+    f0_prepare_kernel<<<grid, kPrepThreads, 0, st>>>(units_dev, frags_dev, m, g, mu, nesterov,
+                                                     reinterpret_cast<float*>(ws + c.part_off),
+                                                     reinterpret_cast<uint16_t*>(ws + c.x_off[0]), c.m, c.n, c.np);
     return cudaGetLastError();
 }
 

@@ -221,14 +221,19 @@ typedef struct {  /* device roots, each in the chain's emulated layout */
 #define HM_STAGE_ALL_FUSED 63
 /* u and v as scratch (section 3.1, EG1: both are update-scoped intermediates,
  * u consumed by f1 and v by f2).  HM_STAGE_SCRATCH requires HM_STAGE_FUSED,
- * and NS only together with F2 and REQUANT (else HM_ERR_ARG).  With F0, the u
- * of straddling units is written to their staging only (the u root keeps its
- * previous contents there).  With NS, the last Newton-Schulz product of every
+ * and NS only together with F2 and REQUANT (else HM_ERR_ARG).  With F0, u is
+ * not written anywhere: f0 runs inside the pass that lays out each shape
+ * class's Newton-Schulz input X0 = u in the workspace (with the norm's partial
+ * sums and the unit scales), reading g and m -- and writing m -- in the rank
+ * segments that hold them, so the fragment gather needs no pass either; the
+ * next NS stage on this plan (with or without SCRATCH) starts from that input
+ * instead of preparing it from the u root.  An F0 stage without SCRATCH, or
+ * muon_plan_upload, drops the prepared input.  With NS, the last Newton-Schulz product of every
  * unit whose cols and fragments are multiples of HM_MX_BLOCK applies f2 and G
  * to that unit in its epilogue, reading w and writing w, q and s directly, and
  * stores no v for it (v keeps its previous contents); the fused F2 + REQUANT
  * pass then covers only the other units (a call with F2 and REQUANT but without
- * NS runs the pass over every unit, from v).  m, w, q, s and the u of local units
+ * NS runs the pass over every unit, from v).  m, v (where written), w, q and s
  * equal those of HM_STAGE_ALL_FUSED bit for bit.  HM_STAGE_STEP is the whole
  * update phase in this fastest form; it may also be split into
  * F0 | GATHER | FUSED | SCRATCH and NS | F2 | REQUANT | FUSED | SCRATCH. */

@@ -39,12 +39,12 @@ def _sample_units(cfg, s, hm, rng):
 
 @pytest.mark.parametrize("name", ["lm_layer", "moe_layer", "video_dit"])
 def test_fullsize_update_sampled(hm, dev, name):
-    """The benchmark's stage set (HM_STAGE_STEP: u of straddling units in
-    their staging only, f2 and G in the last product's epilogue, no v)
-    against the same update through v (HM_STAGE_ALL_FUSED) on a second
-    session: m, w, q, s and u (straddling units from their staging) equal
-    bit for bit over the whole tensor list; the second session's u and v then
-    carry the f0, Newton-Schulz and f2 checks."""
+    """The benchmark's stage set (HM_STAGE_STEP: f0 inside the Newton-Schulz
+    input pass, f2 and G in the last product's epilogue, neither u nor v
+    stored) against the same update through v (HM_STAGE_ALL_FUSED) on a
+    second session: m, w, q, s equal bit for bit over the whole tensor list;
+    the second session's u and v then carry the f0, Newton-Schulz and f2
+    checks."""
     from head_muon_mxfp8_gb300.session import MuonSession, muon_hparams
     cfg = workloads.get(name)
     rng = np.random.default_rng(7)
@@ -74,14 +74,12 @@ def test_fullsize_update_sampled(hm, dev, name):
         if a.dtype == torch.float32:  # bit patterns: the guard words between segments are NaNs
             a, b = a.view(torch.int32), b.view(torch.int32)
         assert torch.equal(a, b), f"{f}: HM_STAGE_STEP differs from the pass through v"
-    u_step, u_v = s.fetch("u"), s_v.fetch("u")
+    u_v = s_v.fetch("u")
     for i, un in enumerate(cfg.units):
         if not hm.muon_plan_unit(s.plan, i)["local"]:
             sl = slice(un.offset, un.offset + un.numel)
-            u_step[sl] = s.staging(i)[0].cpu()
             assert torch.equal(s_v.staging(i)[0].cpu(), u_v[sl])
-    assert torch.equal(u_step, u_v), "u: HM_STAGE_STEP differs from the pass through v"
-    del u_step, u_v
+    del u_v
     # f0 on sampled elements (bit-exact)
     m_ref, u_ref = OM.momentum(m0_s, g_s, cfg.muon.momentum)
     m_all = s.fetch("m")
