@@ -81,12 +81,12 @@ def straddling_elems(cfg, plan_info) -> int:
 
 
 # DRAM bytes (read + write) of one Newton-Schulz stage of the Video-DiT x8
-# workload with f2 and G folded into its last products: an ncu launch list of
-# dram__bytes_read.sum + dram__bytes_write.sum over the timed update of one
-# Video-DiT layer (prepare, norm, the one-launch head-class kernel and 15
-# CTA-pair GEMMs: 19.89 GB), scaled by the units processed (x8); valid only
-# for the kernel source it was measured on (sha256 prefix of hm_ns.cu).
-NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.591e+11, "hm_ns_sha256": "a9bfd7c4d85394d0",
+# workload with f2 and G folded into its last products (the timed update's
+# second call: the one-launch head-class kernel and 15 CTA-pair GEMMs): an ncu
+# launch list of dram__bytes_read.sum + dram__bytes_write.sum over the timed
+# update of one Video-DiT layer (18.91 GB), scaled by the units processed (x8);
+# valid only for the kernel source it was measured on (sha256 prefix of hm_ns.cu).
+NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.512e+11, "hm_ns_sha256": "e7e234de2c25e25e",
                     "how": "one Video-DiT layer measured, x8 by units"}
 
 
@@ -476,9 +476,10 @@ def run_ours(args, cfg):
     roofline = {"bound": "tensor", "achieved": ns_tflops, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                 "frac": ns_tflops / peaks["bf16_sustained"], "traffic": ns_stage_traffic(cfg),
                 "traffic_unit": "DRAM bytes per Newton-Schulz stage (one update), ncu: " + NS_STAGE_TRAFFIC["how"],
-                "kernel": "Newton-Schulz stage: per shape class prepare + norm, then ns_small_kernel (Gram size "
+                "kernel": "Newton-Schulz stage (the step's second call): per shape class ns_small_kernel (Gram size "
                           "128: every iteration in one launch) or ns_gemm_kernel / ns_gemm_pair_kernel (3 products "
-                          "x 5 iterations); the last product also applies f2 and the MXFP8 requant (timed with them)",
+                          "x 5 iterations); the last product also applies f2 and the MXFP8 requant (timed with them); "
+                          "X0 and the unit scales come from the first call (f0 inside the input pass)",
                 "peak_kind": f"bf16 dense sustained ({peaks['source']})",
                 "frac_of_burst": ns_tflops / peaks["bf16"],
                 "note": "achieved counts the algorithmic 5(4m^2n+2m^3) FLOP per unit; the kernels skip the "
@@ -810,6 +811,7 @@ def bench_other_configs(dev, stream, peaks, steps: int = 10, warmup: int = 3):
     for name, k in (("tiny", 50), ("lm_layer", steps), ("moe_layer", steps)):
         cfg = workloads.get(name)
         t = time_muon_update(cfg, dev, stream, k, warmup)
+        classes = ns_class_table(cfg, dev, stream, peaks) if name == "lm_layer" else {}
         P = cfg.numel
         alg = ns_flops(cfg, cfg.muon.ns_steps)
         exe = ns_executed_flops(cfg, cfg.muon.ns_steps)
@@ -829,6 +831,7 @@ def bench_other_configs(dev, stream, peaks, steps: int = 10, warmup: int = 3):
             "f0_gather_fused": {"gbs": 14.0 * P / (t["f0_gather_ms"] / 1e3) / 1e9,
                                 "frac": 14.0 * P / (t["f0_gather_ms"] / 1e3) / 1e9 / peaks["hbm_gbs"]},
             "gpu_launches_per_step": t["launches_per_step"], "clocks": t["clocks"], "cpu_baseline": cpu,
+            "ns_classes": classes,
             "l2": ("inputs larger than L2" if P * 21 > 129e6 else
                    "state fits in L2 (no flush between steps; launch-bound)")}
     out["flat_adamw"] = bench_flat_adamw_config(dev, stream, peaks)
