@@ -1346,20 +1346,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // Every wait is bounded, as in the GEMM kernels.
 // ---------------------------------------------------------------------------
 constexpr int kSmallThreads = 352;
-constexpr int kSmallRing = 4;                // X tiles in flight
-constexpr int kSmallXo = 4;                  // X' tiles in shared memory (written, awaiting the A MMA and the store)
-constexpr int kSmallLag = 2;                 // the A MMA of X'_j is issued after the B X of tile j + kSmallLag
-static_assert(kSmallXo >= kSmallLag + 1 && kSmallXo >= 2, "X' buffers");
 constexpr int kSmallNB = 4;                  // B X accumulators
 constexpr int kSmallTile = 128 * 64 * 2;     // a 128 x 64 bf16 tile (16 KB)
 constexpr int kSmallWGroup = 1;              // w blocks updated together in the last pass (1, 2, 4 measured alike)
+// CS = 1: one CTA per unit.  CS = 2: a unit's tiles split over a CTA pair (a
+// cluster), for classes with fewer units than CTA pairs; each CTA accumulates
+// the part of A from its tiles, and A is formed by adding the two parts over
+// distributed shared memory (below).  RING: X tiles in flight; XO: X' tiles in
+// shared memory (written, awaiting the A MMA and the store); LAG: how many
+// tiles the A MMA of X'_j trails the B X products (LAG 2 with 4 X' tiles
+// measured 2 % faster than LAG 1 with 2); RECV: the peer's half-band of A.
+template <int CS> struct SmallTraits;
+template <> struct SmallTraits<1> { static constexpr int RING = 4, XO = 4, LAG = 2, RECV = 0; };
+template <> struct SmallTraits<2> { static constexpr int RING = 4, XO = 2, LAG = 1, RECV = 64 * 128 * 4; };
+template <int CS>
 struct SmallCfg {
+    using T = SmallTraits<CS>;
+    static_assert(T::XO >= T::LAG + 1 && T::XO >= 2, "X' buffers");
     static constexpr int RING_OFF = 0;
-    static constexpr int AS_OFF = RING_OFF + kSmallRing * kSmallTile;  // A, bf16: two [128][64] K atoms
+    static constexpr int AS_OFF = RING_OFF + T::RING * kSmallTile;     // A, bf16: two [128][64] K atoms
     static constexpr int BS_OFF = AS_OFF + 2 * kSmallTile;              // B, bf16: the same layout
     static constexpr int XO_OFF = BS_OFF + 2 * kSmallTile;              // X' tiles
-    static constexpr int ST_OFF = XO_OFF + kSmallXo * kSmallTile;       // per epilogue warp a 32 x 32 fp32 tile
-    static constexpr int BAR_OFF = ST_OFF + kEpiWarps * 32 * 32 * 4;
+    static constexpr int ST_OFF = XO_OFF + T::XO * kSmallTile;          // per epilogue warp a 32 x 32 fp32 tile
+    static constexpr int RECV_OFF = ST_OFF + kEpiWarps * 32 * 32 * 4;   // CS = 2: the peer's part of this CTA's band of A
+    static constexpr int BAR_OFF = RECV_OFF + T::RECV;
     static constexpr int SMEM = BAR_OFF + 512 + 1024;
     // kind::f16, D fp32, A and B bf16: M = N = 128 with both operands K-major
     // (A X X^T and A A); M = 128, N = 64 with B MN-major (B X)
@@ -1378,6 +1388,42 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem_cluster() {
+    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+// a 16-byte store into a CTA of the cluster (addr from mapa)
+__device__ __forceinline__ void st_cluster_u4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+// Bounded wait with cluster-scope acquire, for barriers the peer CTA arrives
+// on after writing this CTA's shared memory.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, int32_t* err, volatile int* bail) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_cl(bar, parity)) return true;
+        if (*bail) return false;
+        if (globaltimer() - t0 > kWaitNs) {
+            *bail = 1;
+            if (err) atomicCAS(err, 0, kDevErrTimeout);
+            return false;
+        }
+    }
+}
 __device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // 16-byte chunk c (8 bf16) of row r of a [128][64] bf16 tile written with the
@@ -1473,10 +1519,14 @@ __device__ __forceinline__ void final_update_chunk_buf(const GemmParams& p, cons
     }
 }
 
+template <int CS>
 __global__ void __launch_bounds__(kSmallThreads, 1)
     ns_small_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant__ CUtensorMap tx1,
                     const __grid_constant__ SmallNsParams sp) {
-    using C = SmallCfg;
+    using C = SmallCfg<CS>;
+    constexpr int kSmallRing = C::T::RING;
+    constexpr int kSmallXo = C::T::XO;
+    constexpr int kSmallLag = C::T::LAG;
     const GemmParams& p = sp.g;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1485,6 +1535,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     uint8_t* bs = smem + C::BS_OFF;
     uint8_t* xo = smem + C::XO_OFF;
     float* stg = reinterpret_cast<float*>(smem + C::ST_OFF);
+    uint8_t* recv = smem + C::RECV_OFF;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* x_full = bars;                   // ring slot loaded
     uint64_t* x_emma = x_full + kSmallRing;    // slot released by the Gram MMA (Gram-pass tiles)
@@ -1500,7 +1551,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     uint64_t* b_ready = aa_full + 1;           // B in shared memory
     uint64_t* st_done = b_ready + 1;           // an iteration's X' all in global memory
     uint64_t* drain = st_done + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* recv_full = drain + 1;           // CS = 2: the peer's part of this CTA's band of A has arrived
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_full + 1);
     volatile int* bail = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -1521,7 +1573,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
             mbar_init(smem_u32(&xs_done[b]), 1);
         }
         mbar_init(smem_u32(gram_full), 1);
-        mbar_init(smem_u32(a_ready), kEpiWarps);
+        // CS = 2: every lane of the 4 warps that form each half-band of A, in both CTAs
+        mbar_init(smem_u32(a_ready), CS == 1 ? kEpiWarps : 2 * 4 * 32);
+        mbar_init(smem_u32(recv_full), 4 * 32);
         mbar_init(smem_u32(aa_full), 1);
         mbar_init(smem_u32(b_ready), kEpiWarps);
         mbar_init(smem_u32(st_done), 1);
@@ -1534,13 +1588,19 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CS == 2) cluster_sync_all();  // the peer's barriers are initialised before any remote arrive
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int nt = sp.np / 64;  // tiles per pass
+    const uint32_t crank = CS == 2 ? (cluster_ctarank() & 1u) : 0u;
+    const int cid = static_cast<int>(blockIdx.x) / CS, ncl = static_cast<int>(gridDim.x) / CS;
+    // this CTA's tiles of every pass: [tbeg, tbeg + nt) of the unit's np / 64
+    const int per = (sp.np / 64 + CS - 1) / CS;
+    const int tbeg = static_cast<int>(crank) * per;
+    const int nt = min(sp.np / 64, tbeg + per) - tbeg;
     const int S = sp.steps;
     // tile of step t of pass k (k = 0: the Gram pass over X0; k = it + 1: iteration it)
-    auto tile_of = [&](int k, int t) { return (sp.reverse && (k & 1)) ? nt - 1 - t : t; };
+    auto tile_of = [&](int k, int t) { return tbeg + ((sp.reverse && (k & 1)) ? nt - 1 - t : t); };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -1549,7 +1609,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
             uint32_t armed = 0, armed_par = 0;
             int pos = 0, sd = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < sp.units && ok; u += gridDim.x) {
+            for (int u = cid; u < sp.units && ok; u += ncl) {
                 for (int k = 0; k <= S && ok; ++k) {
                     const CUtensorMap* map = (k == 0 || ((k - 1) & 1) == 0) ? &tx0 : &tx1;
                     if (k >= 2) {
@@ -1595,7 +1655,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) umma_bf16(t_a, d + 2 * kk, d + 2 * kk, C::IDESC_G, (acc0 || kk) ? 1u : 0u);
             };
-            for (int u = blockIdx.x; u < sp.units && ok; u += gridDim.x) {
+            for (int u = cid; u < sp.units && ok; u += ncl) {
                 for (int t = 0; t < nt; ++t) {
                     const int s = pos % kSmallRing;
                     if (!mbar_wait(smem_u32(&x_full[s]), (pos / kSmallRing) & 1, p.err, bail)) { ok = false; break; }
@@ -1608,7 +1668,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                 if (!(first && p.inject_no_ready)) umma_commit(smem_u32(gram_full));
                 first = false;
                 for (int it = 0; it < S && ok; ++it) {
-                    if (!mbar_wait(smem_u32(a_ready), ar & 1u, p.err, bail)) { ok = false; break; }
+                    if (!(CS == 2 ? mbar_wait_cl(smem_u32(a_ready), ar & 1u, p.err, bail)
+                                  : mbar_wait(smem_u32(a_ready), ar & 1u, p.err, bail))) {
+                        ok = false;
+                        break;
+                    }
                     ++ar;
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(as);
@@ -1675,7 +1739,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         if (lane == 0) {
             int xg = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < sp.units && ok; u += gridDim.x) {
+            for (int u = cid; u < sp.units && ok; u += ncl) {
                 for (int it = 0; it + 1 < S && ok; ++it) {
                     const CUtensorMap* map = ((it + 1) & 1) ? &tx1 : &tx0;
                     for (int t = 0; t < nt; ++t) {
@@ -1703,9 +1767,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         float* stage = stg + ew * 1024;
         const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
         int pos = 0, dpos = 0, xg = 0;
-        uint32_t gf = 0, af = 0;
+        uint32_t gf = 0, af = 0, rf = 0, arc = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < sp.units && ok; u += gridDim.x) {
+        for (int u = cid; u < sp.units && ok; u += ncl) {
             pos += nt;  // the Gram pass's tiles are released by the MMA
             const float usc = p.unit_scale ? p.unit_scale[u] : 1.f;
             for (int it = 0; it < S && ok; ++it) {
@@ -1717,7 +1781,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                 ++gf;
                 tc_fence_after();
                 const float alpha_t = it == 0 ? 1.f * (usc * usc) : 1.f;
-                {
+                if constexpr (CS == 1) {
                     uint32_t r0[32], r1[32];
                     tmem_ld32(tl + h * 64, r0);
                     tmem_ld32(tl + h * 64 + 32, r1);
@@ -1734,11 +1798,69 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                             bf16x2_bits(__uint_as_float(r[4]) * alpha_t, __uint_as_float(r[5]) * alpha_t),
                             bf16x2_bits(__uint_as_float(r[6]) * alpha_t, __uint_as_float(r[7]) * alpha_t));
                     }
+                    fence_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(a_ready));
+                } else {
+                    // A is the sum of the two CTAs' parts.  CTA r forms rows 64r..64r+63
+                    // (TMEM quadrants 2r, 2r+1): the warps of the other two quadrants send
+                    // their part of those rows to the peer, the warps of its own two add
+                    // the peer's part to theirs, round, and write the band into both CTAs'
+                    // A.  Each band is added by one CTA, so both hold the same A.
+                    const uint32_t peer = crank ^ 1u;
+                    const bool mine = static_cast<uint32_t>(q >> 1) == crank;
+                    const int brow = (q & 1) * 32 + lane;  // row inside the band
+                    const int sw = lane & 15;              // 16-byte chunk swizzle of the receive rows
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tl + h * 64, r0);
+                    tmem_ld32(tl + h * 64 + 32, r1);
+                    tmem_ld_wait();
+                    tmem_ld_pin(r0);
+                    tmem_ld_pin(r1);
+                    if (!mine) {
+                        const uint32_t rb = mapa_shared(smem_u32(recv + brow * 512 + h * 256), peer);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const uint32_t* r = c < 8 ? r0 + 4 * c : r1 + 4 * (c - 8);
+                            st_cluster_u4(rb + ((c ^ sw) << 4), make_uint4(r[0], r[1], r[2], r[3]));
+                        }
+                        mbar_arrive_cluster(mapa_shared(smem_u32(recv_full), peer));
+                    } else {
+                        ok = mbar_wait_cl(smem_u32(recv_full), rf & 1u, p.err, bail);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        ++rf;
+                        const uint8_t* rb = recv + brow * 512 + h * 256;
+                        uint8_t* dst = as + h * kSmallTile;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint32_t* r = c < 4 ? r0 + 8 * c : r1 + 8 * (c - 4);
+                            const float4 x0 = *reinterpret_cast<const float4*>(rb + (((2 * c) ^ sw) << 4));
+                            const float4 x1 = *reinterpret_cast<const float4*>(rb + (((2 * c + 1) ^ sw) << 4));
+                            const float o[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                            float a8[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) a8[e] = (__uint_as_float(r[e]) + o[e]) * alpha_t;
+                            const uint4 v = make_uint4(bf16x2_bits(a8[0], a8[1]), bf16x2_bits(a8[2], a8[3]),
+                                                       bf16x2_bits(a8[4], a8[5]), bf16x2_bits(a8[6], a8[7]));
+                            const uint32_t off = static_cast<uint32_t>(h * kSmallTile) + tile_chunk(row, c);
+                            *reinterpret_cast<uint4*>(dst + tile_chunk(row, c)) = v;
+                            st_cluster_u4(mapa_shared(smem_u32(as) + off, peer), v);
+                        }
+                        fence_async_smem();
+                        fence_async_smem_cluster();
+                        mbar_arrive(smem_u32(a_ready));
+                        mbar_arrive_cluster(mapa_shared(smem_u32(a_ready), peer));
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    // the whole of A (half of it written by the peer) before B is formed from it
+                    ok = mbar_wait_cl(smem_u32(a_ready), arc & 1u, p.err, bail);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    ++arc;
                 }
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(a_ready));
                 // B = bA + cAA, bf16, into shared memory
                 ok = mbar_wait(smem_u32(aa_full), af & 1u, p.err, bail);
                 ok = __all_sync(0xffffffffu, ok);
@@ -1879,27 +2001,56 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         }
         cp_async_wait_all();
     }
-    __syncthreads();
+    if constexpr (CS == 2) {
+        // the peer may still write this CTA's shared memory or arrive on its
+        // barriers: both CTAs stay until every role of both is done
+        __syncwarp();
+        tc_fence_before();
+        cluster_sync_all();
+    } else {
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
 }
 
-cudaError_t launch_small(const CUtensorMap& x0, const CUtensorMap& x1, const SmallNsParams& sp, cudaStream_t st) {
+template <int CS>
+cudaError_t launch_small_cs(const CUtensorMap& x0, const CUtensorMap& x1, const SmallNsParams& sp, cudaStream_t st) {
+    using C = SmallCfg<CS>;
     static bool configured[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SmallCfg::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(ns_small_kernel<CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    if (sp.units == 0) return cudaSuccess;
-    const int grid = sp.units < device_sm_count() ? sp.units : device_sm_count();
+    const int cap = device_sm_count() / CS;
+    const int clusters = sp.units < cap ? sp.units : cap;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CS * clusters, 1, 1);
+    cfg.blockDim = dim3(kSmallThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CS == 2 ? 1 : 0;
     note_launch();
-    ns_small_kernel<<<grid, kSmallThreads, SmallCfg::SMEM, st>>>(x0, x1, sp);
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, ns_small_kernel<CS>, x0, x1, sp);
+}
+
+// A class with at most one unit per CTA pair splits each unit over a pair
+// (when its units have at least two tiles per pass); otherwise one CTA per unit.
+cudaError_t launch_small(const CUtensorMap& x0, const CUtensorMap& x1, const SmallNsParams& sp, cudaStream_t st) {
+    if (sp.units == 0) return cudaSuccess;
+    const bool split = sp.np / 64 >= 2 && 2 * sp.units <= device_sm_count();
+    return split ? launch_small_cs<2>(x0, x1, sp, st) : launch_small_cs<1>(x0, x1, sp, st);
 }
 
 template <bool B_MN>

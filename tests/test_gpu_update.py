@@ -156,7 +156,8 @@ U_UNTOUCHED = np.uint16(0xFFB1)      # a bf16 NaN pattern
 
 @pytest.mark.parametrize("name,variant", [("tiny", "plain"), ("tiny_ragged", "plain"), ("mixed", "plain"),
                                           ("mixed", "decay_alpha"), ("moe_small", "plain"),
-                                          ("ragged_n", "decay_alpha")])
+                                          ("ragged_n", "decay_alpha"), ("mixed", "nesterov"),
+                                          ("ragged_n", "nesterov")])
 def test_fused_update_equals_unfused(hm, dev, name, variant):
     """HM_STAGE_ALL_FUSED (gather folded into f0; f2 and G in one pass) gives
     bit-identical m, u, v, w, q, s to the unfused stages, over two
@@ -178,6 +179,9 @@ def test_fused_update_equals_unfused(hm, dev, name, variant):
         cfg = workloads.get(name)
     if variant == "decay_alpha":
         cfg.muon = dataclasses.replace(cfg.muon, weight_decay=0.1, alpha_mode=2, lr=float(np.float32(0.02)))
+    elif variant == "nesterov":
+        cfg.muon = dataclasses.replace(cfg.muon, nesterov=True, weight_decay=0.1, alpha_mode=1,
+                                       lr=float(np.float32(0.02)))
     data = workloads.generate(cfg, seed=17)
     grads = [data["g"], workloads.gaussian(cfg.numel, cfg.g_std, seed=19)]
     m0 = workloads.gaussian(cfg.numel, 1e-3, seed=18)
