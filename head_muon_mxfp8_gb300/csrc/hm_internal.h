@@ -133,6 +133,7 @@ struct GemmParams {
 struct SmallNsParams {
     GemmParams g;
     int32_t units;    // units of the class
+    int32_t u0;       // first unit this launch takes (units u0 .. units - 1; launch_ns_small sets it)
     int32_t np;       // padded row length of X (multiple of 64)
     int32_t steps;    // Newton-Schulz iterations
     int32_t reverse;  // alternate the tile order of consecutive passes over X

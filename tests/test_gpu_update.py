@@ -439,6 +439,32 @@ def test_newton_schulz_ragged_row_tails(hm, dev):
     s.close()
 
 
+def test_newton_schulz_more_head_units_than_sms(hm, dev):
+    """A Gram-size-128 class with 8 units more than the GPU has SMs: the
+    whole rounds run one unit per CTA, the 8 units of the last round run
+    split over CTA pairs (one launch more), and every unit's v matches the
+    oracle."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cfg = workloads.scaled_muon("heads_tail", [(128, 256, None)] * (sms + 8), so=2, sw=1, sg=1)
+    data = workloads.generate(cfg, seed=23)
+    s = _session(cfg, dev)
+    s.load("w", data["w"])
+    s.load("g", data["g"])
+    s.load("m", np.zeros_like(data["w"]))
+    hp = _hp(cfg.muon)
+    s.run(hp, hm.HM_STAGE_F0 | hm.HM_STAGE_GATHER)
+    before = hm.hm_kernel_launches()
+    s.run(hp, hm.HM_STAGE_NS)
+    n = hm.hm_kernel_launches() - before
+    torch.cuda.synchronize()
+    assert hm.hm_device_error() == 0
+    assert n == 4  # prepare, norm, the whole rounds, the split last round
+    u1 = s.fetch("u").numpy().view(np.uint16)
+    check_ns(cfg, u1, _logical_v(hm, s, cfg), cfg.muon)
+    assert all(s.canary_intact().values())
+    s.close()
+
+
 @pytest.mark.parametrize("steps", [1, 2])
 def test_newton_schulz_iteration_counts(hm, dev, steps):
     """One iteration (the first iteration's 1 / (||u|| + eps) scale lands in
