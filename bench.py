@@ -84,9 +84,9 @@ def straddling_elems(cfg, plan_info) -> int:
 # workload with f2 and G folded into its last products (the timed update's
 # second call: the one-launch head-class kernel and 15 CTA-pair GEMMs): an ncu
 # launch list of dram__bytes_read.sum + dram__bytes_write.sum over the timed
-# update of one Video-DiT layer (18.86 GB), scaled by the units processed (x8);
+# update of one Video-DiT layer (18.84 GB), scaled by the units processed (x8);
 # valid only for the kernel source it was measured on (sha256 prefix of hm_ns.cu).
-NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.509e+11, "hm_ns_sha256": "dbc383eb215793ba",
+NS_STAGE_TRAFFIC = {"workload": "video_dit", "bytes": 1.507e+11, "hm_ns_sha256": "ac4f979a729147d1",
                     "how": "one Video-DiT layer measured, x8 by units"}
 
 
