@@ -24,15 +24,22 @@ def dev(hm):
     return torch.device("cuda:0")
 
 
-@pytest.mark.parametrize("name", ["tiny", "pair", "paced"])
+@pytest.mark.parametrize("name", ["tiny", "heads1", "single", "pair", "paced"])
 def test_injected_wait_timeout_is_reported_and_recovered(hm, dev, name):
-    """tiny: the first GEMM is a single-CTA launch (128-row class); pair: a
-    512 x 768 class, whose GEMMs run on CTA pairs (cta_group::2); paced: two
-    256 x 139264 units, whose X (71 MB each) is more than half the L2, so
-    the pairs also wait on each other's progress (bounded) while the
+    """tiny: 12 units of Gram size 128 on the one-launch kernel, each unit
+    split over a CTA pair (the Gram pass never marks A ready, the peer waits
+    on cluster barriers); heads1: 100 such units, one CTA each; single: a
+    384 x 640 class on the single-CTA GEMM (Gram size not a multiple of 256);
+    pair: a 512 x 768 class, whose GEMMs run on CTA pairs (cta_group::2);
+    paced: two 256 x 139264 units, whose X (71 MB each) is more than half the
+    L2, so the pairs also wait on each other's progress (bounded) while the
     injected wait runs out."""
     from head_muon_mxfp8_gb300.session import MuonSession, muon_hparams
-    if name == "pair":
+    if name == "heads1":
+        cfg = workloads.scaled_muon("heads1", [(64, 128, None)] * 100, so=4, sw=2, sg=2)
+    elif name == "single":
+        cfg = workloads.scaled_muon("single", [(384, 640, None), (640, 384, None)], so=4, sw=2, sg=2)
+    elif name == "pair":
         cfg = workloads.scaled_muon("pair", [(512, 768, None), (768, 512, None)], so=4, sw=2, sg=2)
     elif name == "paced":
         cfg = workloads.scaled_muon("paced", [(256, 139264, None), (139264, 256, None)], so=4, sw=2, sg=2)
