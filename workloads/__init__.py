@@ -164,20 +164,21 @@ def ragged_shift(so: int, max_blocks: int, seed: int) -> List[int]:
     return sh
 
 
-def moe_layer() -> Config:
+def moe_layer(experts: int = 64) -> Config:
     b = _ListBuilder()
-    for e in range(64):
+    for e in range(experts):
         b.add(f"gate{e}", 1408, 2048)
-    for e in range(64):
+    for e in range(experts):
         b.add(f"up{e}", 1408, 2048)
-    for e in range(64):
+    for e in range(experts):
         b.add(f"down{e}", 2048, 1408)
     # even edges would fall exactly on expert boundaries (12 matrices per rank);
     # ragged edges make every one of the 15 interior edges split a matrix
-    return Config("moe_layer", "64 experts, gate/up [1408][2048], down [2048][1408]; "
-                  "192 expert-matrix Muon units; 16 emulated ranks with ragged edges",
+    name = "moe_layer" if experts == 64 else f"moe_layer_{experts}e"
+    return Config(name, f"{experts} experts, gate/up [1408][2048], down [2048][1408]; "
+                  f"{3 * experts} expert-matrix Muon units; 16 emulated ranks with ragged edges",
                   "muon", b.members, b.units, so=16, sw=8, sg=8,
-                  edge_shift=ragged_shift(16, 2048, seed=16))
+                  edge_shift=ragged_shift(16, 2048 * experts // 64, seed=16))
 
 
 def video_dit(layers: int = 8) -> Config:
@@ -229,6 +230,9 @@ CONFIGS = {
     "flat_adamw": flat_adamw,
     "lm_layer": lm_layer,
     "moe_layer": moe_layer,
+    # a quarter of the MoE layer (48 units, about 3 GB on the device): the
+    # same Newton-Schulz shape class, small enough for a multi-pass profiler capture
+    "moe_layer_16e": lambda: moe_layer(16),
     "video_dit": video_dit,
     "video_dit_layer": video_dit_layer,
 }
