@@ -26,12 +26,16 @@ def dev(hm):
 
 
 def _sample_units(cfg, s, hm, rng):
-    """A head (or smallest) unit, a straddling unit and a largest unit."""
+    """A head (or smallest) unit, the last unit of its shape class (with more
+    units than SMs, one that runs in the last round, split over a CTA pair),
+    a straddling unit and a largest unit."""
     sizes = [u.numel for u in cfg.units]
     small = int(np.argmin(sizes))
     big = int(np.argmax(sizes))
+    cls = lambda u: (min(u.rows, u.cols), max(u.rows, u.cols))  # noqa: E731
+    last_small = max(i for i, u in enumerate(cfg.units) if cls(u) == cls(cfg.units[small]))
     strad = [i for i in range(len(cfg.units)) if not hm.muon_plan_unit(s.plan, i)["local"]]
-    pick = {small, big}
+    pick = {small, last_small, big}
     if strad:
         pick.add(int(rng.choice(strad)))
     return sorted(pick)
