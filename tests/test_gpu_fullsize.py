@@ -41,16 +41,22 @@ def _sample_units(cfg, s, hm, rng):
     return sorted(pick)
 
 
-@pytest.mark.parametrize("name", ["lm_layer", "moe_layer", "video_dit"])
-def test_fullsize_update_sampled(hm, dev, name):
+@pytest.mark.parametrize("name,variant", [("lm_layer", "plain"), ("moe_layer", "plain"), ("video_dit", "plain"),
+                                          ("moe_layer", "nesterov_decay")])
+def test_fullsize_update_sampled(hm, dev, name, variant):
     """The benchmark's stage set (HM_STAGE_STEP: f0 inside the Newton-Schulz
     input pass, f2 and G in the last product's epilogue, neither u nor v
     stored) against the same update through v (HM_STAGE_ALL_FUSED) on a
     second session: m, w, q, s equal bit for bit over the whole tensor list;
     the second session's u and v then carry the f0, Newton-Schulz and f2
-    checks."""
+    checks.  nesterov_decay: Nesterov momentum, decoupled weight decay and
+    the shape-dependent step scale sqrt(max(1, rows / cols)) at full size."""
+    import dataclasses
     from head_muon_mxfp8_gb300.session import MuonSession, muon_hparams
     cfg = workloads.get(name)
+    if variant == "nesterov_decay":
+        cfg.muon = dataclasses.replace(cfg.muon, nesterov=True, weight_decay=0.1, alpha_mode=1,
+                                       lr=float(np.float32(0.02)))
     rng = np.random.default_rng(7)
     s = MuonSession.from_config(cfg, device=dev)
     s_v = MuonSession.from_config(cfg, device=dev)
@@ -85,7 +91,7 @@ def test_fullsize_update_sampled(hm, dev, name):
             assert torch.equal(s_v.staging(i)[0].cpu(), u_v[sl])
     del u_v
     # f0 on sampled elements (bit-exact)
-    m_ref, u_ref = OM.momentum(m0_s, g_s, cfg.muon.momentum)
+    m_ref, u_ref = OM.momentum(m0_s, g_s, cfg.muon.momentum, cfg.muon.nesterov)
     m_all = s.fetch("m")
     u_all = s_v.fetch("u")
     assert np.array_equal(m_all[idx.cpu()].numpy().view(np.uint32), m_ref.view(np.uint32))
@@ -101,7 +107,7 @@ def test_fullsize_update_sampled(hm, dev, name):
         err = np.linalg.norm(v.astype(np.float64) - ref.ravel()) / np.linalg.norm(ref)
         assert err <= NS_TOL, f"unit {i} {un.rows}x{un.cols}: {err:.3e}"
         w1 = s.fetch_range("w", un.offset, un.offset + un.numel).numpy()
-        want = OM.main_weight_update(w0_units[i], v, h.lr, 1.0)
+        want = OM.main_weight_update(w0_units[i], v, h.lr, OM.alpha(h.alpha_mode, un.rows, un.cols), h.weight_decay)
         assert np.array_equal(w1.view(np.uint32), want.view(np.uint32))
     del m_all, u_all
     assert all(s_v.canary_intact().values())
